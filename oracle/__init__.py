@@ -1,0 +1,9 @@
+"""CPU float64 oracle of Attn-QAT (NVFP4 fake-quantized attention).
+
+TEST INFRASTRUCTURE ONLY: ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` are the only callers. It shares no code with
+the CUDA path in ``fp4_quantization_aware_gb300``, and neither imports the
+other.
+"""
+from .nvfp4 import fake_nvfp4, fl32, group_scale, quantize_with_scale, rne_e2m1, rne_e4m3  # noqa: F401
+from .attn import attn_qat_bwd, attn_qat_fwd, bwd_head, delta, fwd_head, hats, p_hat, probs  # noqa: F401

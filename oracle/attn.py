@@ -1,0 +1,152 @@
+"""Attn-QAT forward and backward: the oracle (float64, CPU, row-blocked).
+
+TEST INFRASTRUCTURE ONLY. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this module. The library's CUDA
+path never calls it, and it shares no code with that path.
+
+Equations ("NVFP4 Attention QAT Backward", cuDNN frontend docs, *Overview*):
+
+    Q^, K^, V^ = fake_nvfp4(Q), fake_nvfp4(K), fake_nvfp4(V)   (groups along D)
+    P  = softmax(scale * Q^ K^T)
+    O' = P V^                                   (high-precision auxiliary output)
+    dS = P * (dO V^T - rowsum(O' * dO))
+    dQ = scale * dS K^
+    dK = scale * dS^T Q^
+    dV = fake_nvfp4(P)^T dO                     (groups of 16 keys)
+
+and the low-precision forward output of the Attn-QAT paper summary (*Method*):
+``O = fake_nvfp4(P) V^``. The LSE statistic is the natural-log log-sum-exp of
+the scaled logits (cuDNN page, *High-level wrapper*), and the backward
+recomputes P from it (paper summary, Fix 2). Causal masking drops keys j > i
+(self-attention only, cuDNN page *Current support and limitations*).
+
+Inputs are float64 arrays holding BF16-exact values (and an FP32 LSE in the
+backward). P is rounded once to FP32 before it is fake-quantized, because the
+quantizer's definition takes FP32 operands. Outputs are float64 and unrounded;
+tests round O, O' to BF16 and LSE to FP32 where the CUDA path stores them so.
+
+Parity pins (tests/test_oracle_attn.py): torch SDPA in float64 with the
+quantizer set to identity; central finite differences of the STE surrogate
+for dQ and dK; linearity in V^ for dV; the FlashAttention identity
+rowsum(P * dO V^T) = rowsum(O' * dO); the causal first row in closed form;
+a pure-Python brute force on a tiny ragged case.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .nvfp4 import fake_nvfp4, fl32
+
+ROW_BLOCK = 256
+
+
+def _identity(x, axis=-1):
+    return np.asarray(x, dtype=np.float64)
+
+
+def _quantizer(quantize: bool):
+    return fake_nvfp4 if quantize else _identity
+
+
+def p_hat(p, quantize: bool = True):
+    """fake_nvfp4 of the probabilities in groups of 16 keys (FP32 operands).
+
+    With ``quantize=False`` the quantizer, including the FP32 rounding of its
+    operands, is the identity, and the method reduces to textbook attention."""
+    return fake_nvfp4(fl32(p), axis=1) if quantize else np.asarray(p, np.float64)
+
+
+def hats(q, k, v, quantize: bool = True):
+    """Q^, K^, V^: fake-quantized along the head dimension."""
+    f = _quantizer(quantize)
+    return f(q, axis=-1), f(k, axis=-1), f(v, axis=-1)
+
+
+def _logits(qh_blk, kh, scale, causal, row0):
+    s = scale * (qh_blk @ kh.T)
+    if causal:
+        i = np.arange(row0, row0 + qh_blk.shape[0])[:, None]
+        j = np.arange(kh.shape[0])[None, :]
+        s = np.where(j > i, -np.inf, s)
+    return s
+
+
+def probs(qh, kh, scale, causal, lse=None):
+    """Softmax probabilities of one head (Sq, Sk); from ``lse`` if given."""
+    s = _logits(qh, kh, scale, causal, 0)
+    if lse is None:
+        m = np.max(s, axis=1, keepdims=True)
+        lse = (m + np.log(np.sum(np.exp(s - m), axis=1, keepdims=True)))[:, 0]
+    return np.exp(s - np.asarray(lse, np.float64)[:, None])
+
+
+def fwd_head(qh, kh, vh, scale, causal, quantize=True, block=ROW_BLOCK):
+    """One head of the forward on pre-quantized operands: (O, O', LSE)."""
+    Sq = qh.shape[0]
+    o = np.empty((Sq, vh.shape[1]))
+    o_hp = np.empty_like(o)
+    lse = np.empty(Sq)
+    for r0 in range(0, Sq, block):
+        s = _logits(qh[r0:r0 + block], kh, scale, causal, r0)
+        m = np.max(s, axis=1, keepdims=True)
+        l = m + np.log(np.sum(np.exp(s - m), axis=1, keepdims=True))
+        p = np.exp(s - l)
+        o_hp[r0:r0 + block] = p @ vh
+        o[r0:r0 + block] = p_hat(p, quantize) @ vh
+        lse[r0:r0 + block] = l[:, 0]
+    return o, o_hp, lse
+
+
+def bwd_head(do, qh, kh, vh, o_hp, lse, scale, causal, quantize=True, block=ROW_BLOCK):
+    """One head of the backward on pre-quantized operands: (dQ, dK, dV)."""
+    delta = np.sum(o_hp * do, axis=1)
+    dq = np.zeros_like(qh)
+    dk = np.zeros_like(kh)
+    dv = np.zeros_like(vh)
+    for r0 in range(0, qh.shape[0], block):
+        r1 = r0 + block
+        s = _logits(qh[r0:r1], kh, scale, causal, r0)
+        p = np.exp(s - lse[r0:r1, None])
+        dv += p_hat(p, quantize).T @ do[r0:r1]
+        dp = do[r0:r1] @ vh.T
+        ds = p * (dp - delta[r0:r1, None])
+        dq[r0:r1] = scale * (ds @ kh)
+        dk += scale * (ds.T @ qh[r0:r1])
+    return dq, dk, dv
+
+
+def attn_qat_fwd(q, k, v, scale, causal=False, quantize=True):
+    """Forward on BHSD float64 arrays: returns (O, O', LSE) in float64."""
+    q, k, v = (np.asarray(t, np.float64) for t in (q, k, v))
+    if causal and q.shape[2] != k.shape[2]:
+        raise ValueError("causal attention needs Sq == Sk")
+    qh, kh, vh = hats(q, k, v, quantize)
+    B, H, Sq, D = q.shape
+    o = np.empty((B, H, Sq, v.shape[3]))
+    o_hp = np.empty_like(o)
+    lse = np.empty((B, H, Sq))
+    for b in range(B):
+        for h in range(H):
+            o[b, h], o_hp[b, h], lse[b, h] = fwd_head(qh[b, h], kh[b, h], vh[b, h], scale, causal, quantize)
+    return o, o_hp, lse
+
+
+def attn_qat_bwd(do, q, k, v, o_hp, lse, scale, causal=False, quantize=True):
+    """Backward on BHSD float64 arrays: returns (dQ, dK, dV) in float64."""
+    do, q, k, v, o_hp, lse = (np.asarray(t, np.float64) for t in (do, q, k, v, o_hp, lse))
+    if causal and q.shape[2] != k.shape[2]:
+        raise ValueError("causal attention needs Sq == Sk")
+    qh, kh, vh = hats(q, k, v, quantize)
+    dq = np.empty_like(q)
+    dk = np.empty_like(k)
+    dv = np.empty_like(v)
+    for b in range(q.shape[0]):
+        for h in range(q.shape[1]):
+            dq[b, h], dk[b, h], dv[b, h] = bwd_head(do[b, h], qh[b, h], kh[b, h], vh[b, h],
+                                                     o_hp[b, h], lse[b, h], scale, causal, quantize)
+    return dq, dk, dv
+
+
+def delta(o_hp, do):
+    """The backward's preprocessing statistic rowsum(O' * dO), float64."""
+    return np.sum(np.asarray(o_hp, np.float64) * np.asarray(do, np.float64), axis=-1)

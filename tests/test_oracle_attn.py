@@ -1,0 +1,172 @@
+"""Pins of the oracle's Attn-QAT forward and backward.
+
+Each check uses something other than the oracle's own formulas:
+
+* with the quantizer switched to identity the method is textbook attention, so
+  the oracle must match torch's scaled_dot_product_attention and its autograd
+  backward in float64;
+* dQ and dK are the gradients of the STE surrogate <dO, softmax(scale Q^K^T) V^>
+  with respect to Q^ and K^: central finite differences;
+* <dO, fake(P) V^> is linear in V^, so dV = fake(P)^T dO is pinned exactly by a
+  perturbation of V^;
+* the FlashAttention identity rowsum(P * dO V^T) = rowsum(O' * dO) holds exactly
+  for the auxiliary output O' (Attn-QAT paper summary, Fix 1);
+* the first causal row attends only key 0, so P^ of that row is the one-hot
+  group [1.03125, 0, ...] and O_0 = 1.03125 V^_0, O'_0 = V^_0 (closed form);
+* a pure-Python brute force on a tiny ragged case (key groups of 16 + 4) with
+  an enumeration quantizer.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attn, nvfp4
+from fp4_quantization_aware_gb300 import synth
+
+from test_oracle_nvfp4 import brute_group
+
+
+def _inputs(B, H, Sq, Sk, D, seed, gain=1.0):
+    rng = np.random.default_rng(seed)
+    f = lambda *s: synth.bf16_round(rng.standard_normal(s, dtype=np.float32)).astype(np.float64)
+    q = f(B, H, Sq, D) * gain
+    return q, f(B, H, Sk, D), f(B, H, Sk, D), f(B, H, Sq, D)
+
+
+@pytest.mark.parametrize("Sq,Sk,causal", [(40, 40, False), (37, 37, True), (24, 53, False)])
+def test_identity_quantizer_matches_sdpa(Sq, Sk, causal):
+    q, k, v, do = _inputs(2, 3, Sq, Sk, 16, 11)
+    scale = 0.3
+    o, o_hp, lse = attn.attn_qat_fwd(q, k, v, scale, causal, quantize=False)
+    tq, tk, tv = (torch.tensor(t, requires_grad=True) for t in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=causal, scale=scale)
+    ref.backward(torch.tensor(do))
+    np.testing.assert_allclose(o, ref.detach().numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(o_hp, ref.detach().numpy(), rtol=1e-12, atol=1e-12)
+    s = scale * np.einsum("bhid,bhjd->bhij", q, k)
+    if causal:
+        s = np.where(np.triu(np.ones((Sq, Sk), bool), 1), -np.inf, s)
+    np.testing.assert_allclose(lse, torch.logsumexp(torch.tensor(s), -1).numpy(), rtol=1e-13)
+    dq, dk, dv = attn.attn_qat_bwd(do, q, k, v, o_hp, lse, scale, causal, quantize=False)
+    for got, want in ((dq, tq.grad), (dk, tk.grad), (dv, tv.grad)):
+        np.testing.assert_allclose(got, want.numpy(), rtol=1e-10, atol=1e-11)
+
+
+def _surrogate(qh, kh, vh, do, scale, causal):
+    p = attn.probs(qh, kh, scale, causal)
+    return float(np.sum(do * (p @ vh)))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_dq_dk_finite_differences(causal):
+    q, k, v, do = _inputs(1, 1, 33, 33, 16, 12)
+    scale = 1 / 4
+    qh, kh, vh = (nvfp4.fake_nvfp4(t[0, 0]) for t in (q, k, v))
+    do = do[0, 0]
+    o, o_hp, lse = attn.fwd_head(qh, kh, vh, scale, causal)
+    dq, dk, dv = attn.bwd_head(do, qh, kh, vh, o_hp, lse, scale, causal)
+    rng = np.random.default_rng(0)
+    h = 1e-5
+    for target, grad in ((qh, dq), (kh, dk)):
+        for _ in range(25):
+            i, j = rng.integers(target.shape[0]), rng.integers(target.shape[1])
+            old = target[i, j]
+            target[i, j] = old + h
+            lp = _surrogate(qh, kh, vh, do, scale, causal)
+            target[i, j] = old - h
+            lm = _surrogate(qh, kh, vh, do, scale, causal)
+            target[i, j] = old
+            fd = (lp - lm) / (2 * h)
+            assert abs(fd - grad[i, j]) <= 1e-7 * (1 + abs(fd)), (i, j, fd, grad[i, j])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_dv_is_exact_gradient_in_vhat(causal):
+    q, k, v, do = _inputs(1, 1, 48, 48, 16, 13, gain=3.0)
+    scale = 1 / 4
+    qh, kh, vh = (nvfp4.fake_nvfp4(t[0, 0]) for t in (q, k, v))
+    do = do[0, 0]
+    o, o_hp, lse = attn.fwd_head(qh, kh, vh, scale, causal)
+    _, _, dv = attn.bwd_head(do, qh, kh, vh, o_hp, lse, scale, causal)
+    assert np.abs(o).max() > 0.1                  # P^ is not all zero here
+    e = np.random.default_rng(1).standard_normal(vh.shape)
+    o2, _, _ = attn.fwd_head(qh, kh, vh + e, scale, causal)
+    lhs = float(np.sum(do * (o2 - o)))
+    rhs = float(np.sum(dv * e))
+    assert abs(lhs - rhs) <= 1e-11 * (1 + abs(rhs))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_flash_identity_with_auxiliary_output(causal):
+    q, k, v, do = _inputs(1, 1, 64, 64, 32, 14)
+    scale = 1 / math.sqrt(32)
+    qh, kh, vh = (nvfp4.fake_nvfp4(t[0, 0]) for t in (q, k, v))
+    do = do[0, 0]
+    o, o_hp, lse = attn.fwd_head(qh, kh, vh, scale, causal)
+    p = attn.probs(qh, kh, scale, causal)
+    lhs = np.sum(p * (do @ vh.T), axis=1)
+    np.testing.assert_allclose(lhs, np.sum(o_hp * do, axis=1), rtol=1e-12, atol=1e-12)
+    # the identity is broken by the quantized output, which is why O' exists
+    assert np.max(np.abs(lhs - np.sum(o * do, axis=1))) > 1e-3
+
+
+def test_causal_first_row_closed_form():
+    q, k, v, _ = _inputs(1, 2, 20, 20, 16, 15)
+    scale = 0.25
+    o, o_hp, lse = attn.attn_qat_fwd(q, k, v, scale, causal=True)
+    qh, kh, vh = attn.hats(q, k, v)
+    np.testing.assert_array_equal(o[:, :, 0], 1.03125 * vh[:, :, 0])
+    np.testing.assert_allclose(o_hp[:, :, 0], vh[:, :, 0], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(lse[:, :, 0], scale * np.sum(qh[:, :, 0] * kh[:, :, 0], -1), rtol=1e-14)
+
+
+def _brute_attention(q, k, v, do, scale, causal):
+    """Scalar pure-Python Attn-QAT on one head, with the enumeration quantizer."""
+    Sq, D = len(q), len(q[0])
+    Sk = len(k)
+    qh = [list(brute_group(row[g:g + 16])) for row in q for g in range(0, D, 16)]
+    qh = [sum(qh[r * (D // 16):(r + 1) * (D // 16)], []) for r in range(Sq)]
+    kh = [sum((list(brute_group(row[g:g + 16])) for g in range(0, D, 16)), []) for row in k]
+    vh = [sum((list(brute_group(row[g:g + 16])) for g in range(0, D, 16)), []) for row in v]
+    P, Ph, lse = [], [], []
+    for i in range(Sq):
+        s = [scale * sum(qh[i][d] * kh[j][d] for d in range(D)) if not (causal and j > i) else -math.inf
+             for j in range(Sk)]
+        m = max(s)
+        l = m + math.log(sum(math.exp(x - m) for x in s))
+        p = [math.exp(x - l) for x in s]
+        p32 = [float(np.float32(x)) for x in p]
+        ph = []
+        for g in range(0, Sk, 16):
+            seg = p32[g:g + 16]
+            ph += list(brute_group(seg + [0.0] * (16 - len(seg))))[:len(seg)]
+        P.append(p), Ph.append(ph), lse.append(l)
+    O = [[sum(Ph[i][j] * vh[j][d] for j in range(Sk)) for d in range(D)] for i in range(Sq)]
+    Ohp = [[sum(P[i][j] * vh[j][d] for j in range(Sk)) for d in range(D)] for i in range(Sq)]
+    delta = [sum(Ohp[i][d] * do[i][d] for d in range(D)) for i in range(Sq)]
+    dP = [[sum(do[i][d] * vh[j][d] for d in range(D)) for j in range(Sk)] for i in range(Sq)]
+    dS = [[P[i][j] * (dP[i][j] - delta[i]) for j in range(Sk)] for i in range(Sq)]
+    dQ = [[scale * sum(dS[i][j] * kh[j][d] for j in range(Sk)) for d in range(D)] for i in range(Sq)]
+    dK = [[scale * sum(dS[i][j] * qh[i][d] for i in range(Sq)) for d in range(D)] for j in range(Sk)]
+    dV = [[sum(Ph[i][j] * do[i][d] for i in range(Sq)) for d in range(D)] for j in range(Sk)]
+    return [np.array(t) for t in (O, Ohp, lse, dQ, dK, dV)]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_tiny_ragged_brute_force(causal):
+    q, k, v, do = _inputs(1, 1, 20, 20, 16, 16, gain=3.0)
+    scale = 0.5
+    o, o_hp, lse = attn.attn_qat_fwd(q, k, v, scale, causal)
+    dq, dk, dv = attn.attn_qat_bwd(do, q, k, v, o_hp, lse, scale, causal)
+    want = _brute_attention(q[0, 0].tolist(), k[0, 0].tolist(), v[0, 0].tolist(), do[0, 0].tolist(), scale, causal)
+    for got, ref in zip((o, o_hp, lse, dq, dk, dv), want):
+        np.testing.assert_allclose(got[0, 0], ref, rtol=1e-10, atol=1e-12)
+    assert np.count_nonzero(o) > 0
+
+
+def test_rejects_causal_cross_attention():
+    q, k, v, _ = _inputs(1, 1, 8, 12, 16, 17)
+    with pytest.raises(ValueError):
+        attn.attn_qat_fwd(q, k, v, 0.25, causal=True)
