@@ -1,0 +1,177 @@
+"""ctypes binding of libattnqat (the C ABI in include/attnqat.h).
+
+Argument marshalling only: every step of the computation runs in the
+library's CUDA kernels. PyTorch provides device memory and streams. There is
+no fallback: ``load()`` raises if the library has not been built, and every
+non-OK status becomes an ``AttnQatError``.
+
+The raw entry points are available with their C names on the loaded library
+(``load().attnqat_fwd(...)``); the functions below wrap them for torch tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libattnqat.so")
+
+ATTNQAT_OK = 0
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "misaligned", 4: "workspace", 5: "cuda",
+          6: "timeout"}
+
+
+class Problem(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("H", ctypes.c_int64), ("Sq", ctypes.c_int64), ("Sk", ctypes.c_int64),
+                ("D", ctypes.c_int64), ("is_causal", ctypes.c_int32), ("softmax_scale", ctypes.c_float)]
+
+
+class AttnQatError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({status}) {detail}".strip())
+        self.status = status
+
+
+_P = ctypes.c_void_p
+_S = ctypes.c_int
+_PP = ctypes.POINTER(Problem)
+SIGNATURES = {
+    "attnqat_version": (ctypes.c_int, []),
+    "attnqat_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "attnqat_last_error_message": (ctypes.c_char_p, []),
+    "attnqat_check_support": (_S, [_PP]),
+    "attnqat_fwd_workspace_bytes": (ctypes.c_size_t, [_PP]),
+    "attnqat_bwd_workspace_bytes": (ctypes.c_size_t, [_PP]),
+    "attnqat_fake_nvfp4": (_S, [_P, _P, ctypes.c_int64, ctypes.c_int64, _P]),
+    "attnqat_fake_nvfp4_f32": (_S, [_P, _P, ctypes.c_int64, ctypes.c_int64, _P]),
+    "attnqat_fwd": (_S, [_PP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "attnqat_bwd": (_S, [_PP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "attnqat_quantize_qkv": (_S, [_PP, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "attnqat_fwd_main": (_S, [_PP, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "attnqat_bwd_preprocess": (_S, [_PP, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "attnqat_bwd_main": (_S, [_PP, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "attnqat_bwd_dq_convert": (_S, [_PP, _P, _P, ctypes.c_size_t, _P]),
+    "attnqat_device_status": (_S, [ctypes.c_int]),
+    "attnqat_selftest_wait_timeout": (_S, [ctypes.c_uint64, _P]),
+}
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Open the built library (raises if it is missing) and declare signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -m fp4_quantization_aware_gb300.build` "
+                           "(or __graft_entry__.build())")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype, fn.argtypes = res, args
+    _lib = lib
+    return lib
+
+
+def check(status: int, where: str) -> None:
+    if status != ATTNQAT_OK:
+        detail = load().attnqat_last_error_message().decode()
+        raise AttnQatError(status, where, detail)
+
+
+def problem(B, H, Sq, Sk, D, causal=False, scale=None) -> Problem:
+    return Problem(B, H, Sq, Sk, D, 1 if causal else 0, 1.0 / math.sqrt(D) if scale is None else scale)
+
+
+# ------------------------------------------------------------------ torch helpers
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _problem_of(q, k, causal, scale) -> Problem:
+    B, H, Sq, D = q.shape
+    return problem(B, H, Sq, k.shape[2], D, causal, scale)
+
+
+def _bf16_contig(*ts):
+    import torch
+    for t in ts:
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("tensors must be contiguous CUDA bfloat16 (BHSD)")
+
+
+def fake_nvfp4(x, stream=None):
+    """fake_nvfp4 along the last axis (groups of 16) of a BF16 or FP32 CUDA tensor."""
+    import torch
+    x = x.contiguous()
+    y = torch.empty_like(x)
+    cols = x.shape[-1]
+    rows = x.numel() // cols if cols else 0
+    lib = load()
+    if x.dtype == torch.bfloat16:
+        check(lib.attnqat_fake_nvfp4(_ptr(x), _ptr(y), rows, cols, _stream(stream)), "attnqat_fake_nvfp4")
+    elif x.dtype == torch.float32:
+        check(lib.attnqat_fake_nvfp4_f32(_ptr(x), _ptr(y), rows, cols, _stream(stream)), "attnqat_fake_nvfp4_f32")
+    else:
+        raise ValueError("fake_nvfp4 takes bfloat16 or float32")
+    return y
+
+
+def workspace(nbytes: int, device):
+    import torch
+    return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+
+
+def fwd(q, k, v, causal=False, scale=None, ws=None, out=None, stream=None):
+    """Forward: returns (O, O', LSE) for BHSD BF16 CUDA tensors."""
+    import torch
+    _bf16_contig(q, k, v)
+    p = _problem_of(q, k, causal, scale)
+    lib = load()
+    need = lib.attnqat_fwd_workspace_bytes(ctypes.byref(p))
+    if need == 0:
+        check(lib.attnqat_check_support(ctypes.byref(p)), "attnqat_check_support")
+    if ws is None:
+        ws = workspace(need, q.device)
+    if out is None:
+        o, o_hp = torch.empty_like(q), torch.empty_like(q)
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    else:
+        o, o_hp, lse = out
+    check(lib.attnqat_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(o_hp), _ptr(lse), _ptr(ws),
+                          ws.numel(), _stream(stream)), "attnqat_fwd")
+    return o, o_hp, lse
+
+
+def bwd(do, q, k, v, o_hp, lse, causal=False, scale=None, ws=None, out=None, stream=None):
+    """Backward: returns (dQ, dK, dV) for BHSD BF16 CUDA tensors."""
+    import torch
+    _bf16_contig(do, q, k, v, o_hp)
+    p = _problem_of(q, k, causal, scale)
+    lib = load()
+    need = lib.attnqat_bwd_workspace_bytes(ctypes.byref(p))
+    if need == 0:
+        check(lib.attnqat_check_support(ctypes.byref(p)), "attnqat_check_support")
+    if ws is None:
+        ws = workspace(need, q.device)
+    if out is None:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    else:
+        dq, dk, dv = out
+    check(lib.attnqat_bwd(ctypes.byref(p), _ptr(do), _ptr(q), _ptr(k), _ptr(v), _ptr(o_hp), _ptr(lse), _ptr(dq),
+                          _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(), _stream(stream)), "attnqat_bwd")
+    return dq, dk, dv
+
+
+def device_status(clear: bool = True) -> int:
+    """The device error word (0 = ok, 6 = a bounded wait timed out); synchronizes."""
+    return load().attnqat_device_status(1 if clear else 0)

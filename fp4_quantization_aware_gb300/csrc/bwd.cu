@@ -1,0 +1,402 @@
+// Attn-QAT backward main kernel (sm_103a): dK, dV and the dQ contributions.
+//
+// "NVFP4 Attention QAT Backward" (cuDNN frontend docs, Overview):
+//   dS = P * (dO V^T - delta),  delta = rowsum(O' * dO)
+//   dQ = scale * dS K^,  dK = scale * dS^T Q^,  dV = fake_nvfp4(P)^T dO
+// with P recomputed from the forward's LSE ("Attn-QAT" paper summary, Fix 2)
+// and fake-quantized in registers in groups of 16 keys before the P^T dO MMA.
+// dQ and dK use the unquantized P (straight-through estimator).
+//
+// One CTA owns a 128-key tile of one (b, h) and walks the 128-row query tiles
+// (causal: from the diagonal tile on, keeping the element mask on the
+// diagonal; tiles past Sq/Sk are zero-filled by TMA and masked).
+//
+// Per query tile i (all MMAs tcgen05 kind::f16, BF16 in, FP32 in TMEM):
+//   S  = Q^_i K^T        (TMEM cols [0,128), lane = query row)
+//   dP = dO_i V^T        (cols [128,256))
+//   dV += P^T dO_i       (cols [256,256+D), lane = key)   A = P^ from smem (MN-major)
+//   dK += dS^T Q^_i      (cols [256+D,256+2D))            A = dS from smem (MN-major)
+//   dQ_i = dS K^         (reuses the dP columns)          A = dS (K-major)
+// Warp roles (14 warps):
+//   0-7  softmax: P = exp2(S*c - lse2), P^ = fake_nvfp4(P) -> smem, dS -> smem
+//        (warp w reads TMEM lanes 32*(w%4).., columns [64*(w/4), +64) of a tile)
+//   8-11 dQ drain: TMEM -> scaled FP32 -> swizzled smem -> TMA reduce-add into
+//        the workspace's FP32 dQ accumulator (one 32x32 box per warp and chunk)
+//   12   TMA producer (lane 0)
+//   13   MMA issuer (lane 0); the whole warp allocates and frees TMEM
+// Shared memory (D = 128): K^ 32K, V^ 32K, Q^ x2 64K, dO 32K, P^/dS 32K,
+// dQ staging 32K = 224 KiB.
+#include "attn_common.cuh"
+
+namespace attnqat {
+namespace {
+
+constexpr int kThreadsBwd = 14 * 32;
+constexpr int kWarpTma = 12;
+constexpr int kWarpMma = 13;
+constexpr int kWarpDq0 = 8;
+
+template <int D>
+struct BwdLayout {
+  static constexpr uint32_t kTile = 128 * D * 2;
+  static constexpr uint32_t kK = 0;
+  static constexpr uint32_t kV = kK + kTile;
+  static constexpr uint32_t kQ0 = kV + kTile;
+  static constexpr uint32_t kQ1 = kQ0 + kTile;
+  static constexpr uint32_t kDO = kQ1 + kTile;
+  static constexpr uint32_t kPS = kDO + kTile;          // 128 x 128 BF16
+  static constexpr uint32_t kDQ = kPS + 2 * kBlockBytes; // 4 warps x 2 stages x 4 KiB
+  static constexpr uint32_t kBar = kDQ + 32768;
+  static constexpr uint32_t kBytes = kBar + 256;
+  static constexpr uint32_t kAlloc = kBytes + 1024;      // room to align the base to 1024
+  // TMEM columns
+  static constexpr uint32_t kColS = 0;
+  static constexpr uint32_t kColDP = 128;
+  static constexpr uint32_t kColDV = 256;
+  static constexpr uint32_t kColDK = 256 + D;
+};
+
+struct BwdBars {
+  uint64_t kv_full;
+  uint64_t q_full[2];
+  uint64_t q_empty[2];
+  uint64_t do_full;
+  uint64_t do_empty;
+  uint64_t s_full;
+  uint64_t s_free;
+  uint64_t dp_full;
+  uint64_t dp_free;
+  uint64_t p_ready;
+  uint64_t dv_done;
+  uint64_t ds_ready;
+  uint64_t buf_free;
+  uint64_t dq_full;
+  uint64_t drain;
+  uint32_t tmem_base;
+  uint32_t abort_flag;
+};
+
+struct BwdArgs {
+  const float* lse;
+  const float* delta;
+  bf16* dk;
+  bf16* dv;
+  int Sq, Sk;
+  int n_qtiles;
+  int causal;
+  float scale;
+  float c2;   // scale * log2(e)
+  uint32_t* err;
+  uint64_t timeout_ns;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreadsBwd, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+               const __grid_constant__ CUtensorMap tm_dq, const BwdArgs a) {
+  using L = BwdLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  BwdBars& B = *reinterpret_cast<BwdBars*>(smem + L::kBar);
+
+  const int warp = warp_id();
+  const int lane = lane_id();
+  const int j = blockIdx.x;                 // key tile
+  const int bh = blockIdx.y;
+  const int i_begin = a.causal ? j : 0;     // BM == BN: the diagonal tile index equals j
+  const int n_it = a.n_qtiles - i_begin;
+
+  if (threadIdx.x == 0) {
+    B.abort_flag = 0;
+    mbar_init(&B.kv_full, 1);
+    for (int s = 0; s < 2; ++s) mbar_init(&B.q_full[s], 1), mbar_init(&B.q_empty[s], 1);
+    mbar_init(&B.do_full, 1);
+    mbar_init(&B.do_empty, 1);
+    mbar_init(&B.s_full, 1);
+    mbar_init(&B.s_free, 256);
+    mbar_init(&B.dp_full, 1);
+    mbar_init(&B.dp_free, 128);
+    mbar_init(&B.p_ready, 256);
+    mbar_init(&B.dv_done, 1);
+    mbar_init(&B.ds_ready, 256);
+    mbar_init(&B.buf_free, 1);
+    mbar_init(&B.dq_full, 1);
+    mbar_init(&B.drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(&B.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = B.tmem_base;
+  const WaitCtl ctl{&B.abort_flag, a.err, a.timeout_ns};
+
+  if (warp == kWarpTma) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q), tma_prefetch_desc(&tm_k), tma_prefetch_desc(&tm_v), tma_prefetch_desc(&tm_do);
+      int q_uses[2] = {0, 0}, do_uses = 0;
+      mbar_arrive_expect_tx(&B.kv_full, 2 * L::kTile);
+      for (int b = 0; b < D / 64; ++b) {
+        tma_load_3d(smem + L::kK + b * kBlockBytes, &tm_k, &B.kv_full, b * 64, j * 128, bh);
+        tma_load_3d(smem + L::kV + b * kBlockBytes, &tm_v, &B.kv_full, b * 64, j * 128, bh);
+      }
+      for (int it = 0; it < n_it; ++it) {
+        const int i = i_begin + it, s = it & 1;
+        if (it >= 2 && !mbar_wait(&B.q_empty[s], ((it >> 1) - 1) & 1, ctl)) break;
+        mbar_arrive_expect_tx(&B.q_full[s], L::kTile);
+        for (int b = 0; b < D / 64; ++b)
+          tma_load_3d(smem + (s ? L::kQ1 : L::kQ0) + b * kBlockBytes, &tm_q, &B.q_full[s], b * 64, i * 128, bh);
+        ++q_uses[s];
+        if (it >= 1 && !mbar_wait(&B.do_empty, (it - 1) & 1, ctl)) break;
+        mbar_arrive_expect_tx(&B.do_full, L::kTile);
+        for (int b = 0; b < D / 64; ++b)
+          tma_load_3d(smem + L::kDO + b * kBlockBytes, &tm_do, &B.do_full, b * 64, i * 128, bh);
+        ++do_uses;
+      }
+      // Let every copy this CTA issued land before shared memory is released.
+      mbar_wait_drain(&B.kv_full, 0, ctl);
+      for (int s = 0; s < 2; ++s)
+        if (q_uses[s]) mbar_wait_drain(&B.q_full[s], (q_uses[s] - 1) & 1, ctl);
+      if (do_uses) mbar_wait_drain(&B.do_full, (do_uses - 1) & 1, ctl);
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);   // S, dP
+      constexpr uint32_t kIdT = idesc_bf16(128, D, true, true);       // dV, dK
+      constexpr uint32_t kIdQ = idesc_bf16(128, D, false, true);      // dQ
+      // X[128 x 128] = A[128 x D] B[128 x D]^T, both K-major (K = D).
+      auto mma_nt = [&](uint32_t a_off, uint32_t b_off, uint32_t col) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t o = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
+          umma_bf16(tmem + col, sdesc_sw128(sbase + a_off + o, 16, 1024), sdesc_sw128(sbase + b_off + o, 16, 1024),
+                    kIdS, kk > 0);
+        }
+      };
+      // X[128 keys x D] (+)= A^T B with A = [128 q x 128 keys] and B = [128 q x D],
+      // both read MN-major (K = 128 query rows, 16 per step).
+      auto mma_tn = [&](uint32_t a_off, uint32_t b_off, uint32_t col, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t o = kk * 2048;
+          umma_bf16(tmem + col, sdesc_sw128(sbase + a_off + o, kBlockBytes, 1024),
+                    sdesc_sw128(sbase + b_off + o, kBlockBytes, 1024), kIdT, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      // dQ[128 q x D] = dS[128 q x 128 keys] K^[128 keys x D]: A K-major, B MN-major.
+      auto mma_dq = [&]() {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t oa = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
+          const uint32_t ob = kk * 2048;
+          umma_bf16(tmem + L::kColDP, sdesc_sw128(sbase + L::kPS + oa, 16, 1024),
+                    sdesc_sw128(sbase + L::kK + ob, kBlockBytes, 1024), kIdQ, kk > 0);
+        }
+      };
+
+      bool ok = mbar_wait(&B.kv_full, 0, ctl) && mbar_wait(&B.q_full[0], 0, ctl);
+      if (ok) {
+        tc_fence_after();
+        mma_nt(L::kQ0, L::kK, L::kColS);
+        umma_commit(&B.s_full);
+      }
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int s = it & 1;
+        if (!mbar_wait(&B.do_full, it & 1, ctl)) break;
+        if (it >= 1 && !mbar_wait(&B.dp_free, (it - 1) & 1, ctl)) break;
+        tc_fence_after();
+        mma_nt(L::kDO, L::kV, L::kColDP);
+        umma_commit(&B.dp_full);
+
+        if (!mbar_wait(&B.p_ready, it & 1, ctl)) break;
+        tc_fence_after();
+        mma_tn(L::kPS, L::kDO, L::kColDV, it > 0);
+        umma_commit(&B.dv_done);
+        umma_commit(&B.do_empty);
+
+        if (it + 1 < n_it) {
+          const int s1 = (it + 1) & 1;
+          if (!mbar_wait(&B.q_full[s1], ((it + 1) >> 1) & 1, ctl)) break;
+          if (!mbar_wait(&B.s_free, it & 1, ctl)) break;
+          tc_fence_after();
+          mma_nt(s1 ? L::kQ1 : L::kQ0, L::kK, L::kColS);
+          umma_commit(&B.s_full);
+        }
+
+        if (!mbar_wait(&B.ds_ready, it & 1, ctl)) break;
+        tc_fence_after();
+        mma_tn(L::kPS, s ? L::kQ1 : L::kQ0, L::kColDK, it > 0);
+        umma_commit(&B.q_empty[s]);
+        mma_dq();
+        umma_commit(&B.dq_full);
+        umma_commit(&B.buf_free);
+      }
+      // Every MMA issued above completes before TMEM and smem are released.
+      umma_commit(&B.drain);
+      mbar_wait_drain(&B.drain, 0, ctl);
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ softmax / quant
+    const uint32_t quarter = warp & 3, half = warp >> 2;
+    const uint32_t r = quarter * 32 + lane;                  // row of the query tile
+    const uint32_t lane_off = (quarter * 32u) << 16;
+    const uint32_t ps_block = sbase + L::kPS + half * kBlockBytes;
+    const int key0 = j * 128 + half * 64;                    // first key of my 64 columns
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int i = i_begin + it;
+      const int qrow = i * 128 + r;
+      float lse2 = INFINITY, dlt = 0.0f;
+      if (qrow < a.Sq) {
+        lse2 = a.lse[(size_t)bh * a.Sq + qrow] * kLog2e;
+        dlt = a.delta[(size_t)bh * a.Sq + qrow];
+      }
+      const int kend = a.causal ? min(a.Sk, qrow + 1) : a.Sk;
+      const int valid = kend - key0;                         // columns [0, valid) are live keys
+
+      if (!warp_wait(&B.s_full, it & 1, ctl)) { ok = false; break; }
+      tc_fence_after();
+      float P[64];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + L::kColS + half * 64 + c * 32, v);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float p = ex2(fmaf(__uint_as_float(v[k]), a.c2, -lse2));
+          P[c * 32 + k] = (c * 32 + k < valid) ? p : 0.0f;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&B.s_free);
+
+      uint32_t ph[32];
+#pragma unroll
+      for (int g = 0; g < 4; ++g) quant_pack16(P + 16 * g, ph + 8 * g);
+      if (it > 0 && !warp_wait(&B.buf_free, (it - 1) & 1, ctl)) { ok = false; break; }
+      store_row64(ps_block, r, ph);
+      fence_proxy_async_smem();
+      mbar_arrive(&B.p_ready);
+
+      if (!warp_wait(&B.dp_full, it & 1, ctl)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t ds[32];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + L::kColDP + half * 64 + c * 32, v);
+#pragma unroll
+        for (int k = 0; k < 32; k += 2) {
+          const float d0 = P[c * 32 + k] * (__uint_as_float(v[k]) - dlt);
+          const float d1 = P[c * 32 + k + 1] * (__uint_as_float(v[k + 1]) - dlt);
+          ds[c * 16 + k / 2] = pack_bf16x2(d0, d1);
+        }
+      }
+      tc_fence_before();
+      if (!warp_wait(&B.dv_done, it & 1, ctl)) { ok = false; break; }
+      store_row64(ps_block, r, ds);
+      fence_proxy_async_smem();
+      mbar_arrive(&B.ds_ready);
+    }
+    // Epilogue: warps 0-3 write dK (scaled), warps 4-7 write dV, one key row each.
+    if (ok && warp_wait(&B.buf_free, (n_it - 1) & 1, ctl)) {
+      tc_fence_after();
+      const int krow = j * 128 + r;
+      const uint32_t col = half == 0 ? L::kColDK : L::kColDV;
+      const float mul = half == 0 ? a.scale : 1.0f;
+      bf16* out = (half == 0 ? a.dk : a.dv) + ((size_t)bh * a.Sk + krow) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + col + c * 32, v);
+        if (krow < a.Sk) store_row32_bf16(out + c * 32, v, mul);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ dQ drain (warps 8-11)
+    const uint32_t quarter = warp & 3;
+    const uint32_t r = quarter * 32 + lane;
+    const uint32_t lane_off = (quarter * 32u) << 16;
+    const uint32_t stage0 = sbase + L::kDQ + quarter * 8192;   // two 4 KiB stages of 32 rows x 128 B
+    uint8_t* stage0_ptr = smem + L::kDQ + quarter * 8192;
+    int chunk = 0;
+    for (int it = 0; it < n_it; ++it) {
+      const int i = i_begin + it;
+      if (!warp_wait(&B.dq_full, it & 1, ctl)) break;
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c, ++chunk) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + L::kColDP + c * 32, v);
+        if (c == D / 32 - 1) {
+          tc_fence_before();
+          mbar_arrive(&B.dp_free);
+        }
+        const uint32_t b = chunk & 1;
+        if (lane == 0) bulk_wait_group_read<1>();            // the reduce that last read stage b is done
+        __syncwarp();
+        const uint32_t st = stage0 + b * 4096;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          st_shared_v4(sw128_chunk(st, lane, k), __float_as_uint(__uint_as_float(v[4 * k]) * a.scale),
+                       __float_as_uint(__uint_as_float(v[4 * k + 1]) * a.scale),
+                       __float_as_uint(__uint_as_float(v[4 * k + 2]) * a.scale),
+                       __float_as_uint(__uint_as_float(v[4 * k + 3]) * a.scale));
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_reduce_add_3d(&tm_dq, stage0_ptr + b * 4096, c * 32, i * 128 + quarter * 32, bh);
+          bulk_commit_group();
+        }
+      }
+    }
+    if (lane == 0) bulk_wait_group<0>();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const Problem& p, const bf16* qh, const bf16* kh, const bf16* vh, const bf16* dout,
+                       const float* lse, const float* delta, float* dq_acc, bf16* dk, bf16* dv, uint32_t* err,
+                       cudaStream_t st) {
+  CUtensorMap tq, tk, tv, tdo, tdq;
+  const uint64_t bh = p.bh();
+  if (!make_tile_map(&tq, qh, false, p.D, p.Sq, bh, 64, 128) || !make_tile_map(&tk, kh, false, p.D, p.Sk, bh, 64, 128) ||
+      !make_tile_map(&tv, vh, false, p.D, p.Sk, bh, 64, 128) || !make_tile_map(&tdo, dout, false, p.D, p.Sq, bh, 64, 128) ||
+      !make_tile_map(&tdq, dq_acc, true, p.D, p.Sq, bh, 32, 32))
+    return cudaErrorInvalidValue;
+  BwdArgs a;
+  a.lse = lse, a.delta = delta, a.dk = dk, a.dv = dv;
+  a.Sq = static_cast<int>(p.Sq), a.Sk = static_cast<int>(p.Sk);
+  a.n_qtiles = static_cast<int>((p.Sq + kBlockM - 1) / kBlockM);
+  a.causal = p.causal ? 1 : 0;
+  a.scale = p.scale, a.c2 = p.scale * kLog2e;
+  a.err = err, a.timeout_ns = kWaitTimeoutNs;
+  const dim3 grid(static_cast<unsigned>((p.Sk + kBlockN - 1) / kBlockN), static_cast<unsigned>(bh));
+  if (p.D == 128) {
+    cudaError_t e = set_smem(reinterpret_cast<const void*>(&bwd_kernel<128>), BwdLayout<128>::kAlloc);
+    if (e != cudaSuccess) return e;
+    bwd_kernel<128><<<grid, kThreadsBwd, BwdLayout<128>::kAlloc, st>>>(tq, tk, tv, tdo, tdq, a);
+  } else {
+    cudaError_t e = set_smem(reinterpret_cast<const void*>(&bwd_kernel<64>), BwdLayout<64>::kAlloc);
+    if (e != cudaSuccess) return e;
+    bwd_kernel<64><<<grid, kThreadsBwd, BwdLayout<64>::kAlloc, st>>>(tq, tk, tv, tdo, tdq, a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace attnqat

@@ -1,0 +1,350 @@
+// Attn-QAT forward main kernel (sm_103a): O, O' and LSE.
+//
+// "Attn-QAT: 4-Bit Attention With Quantization-Aware Training" (Method, Fix 1)
+// and "NVFP4 Attention QAT Backward" (cuDNN frontend docs, Overview):
+//   P   = softmax(scale * Q^ K^T)  (FP32)
+//   O'  = P V^                     (auxiliary high-precision output, BF16)
+//   O   = fake_nvfp4(P) V^         (groups of 16 keys of the normalised P)
+//   LSE = natural-log log-sum-exp of the scaled logits (FP32)
+//
+// fake_nvfp4 is applied to the normalised probabilities, and fake(c x) differs
+// from c fake(x) unless c is a power of two, so P^ needs the final LSE. The
+// kernel therefore makes two passes over the key tiles of its 128-row query
+// tile: pass 1 computes S and the row max/sum (LSE); pass 2 recomputes S,
+// forms the final P and P^, and accumulates O' and O in TMEM with no
+// rescaling.
+//
+// TMEM columns: S double-buffered [0,128) and [128,256); O' [256,256+D);
+// O [256+D,256+2D). Warp roles (10 warps): 0-7 softmax (warp w: lanes
+// 32*(w%4).., key columns [64*(w/4), +64)); 8 TMA producer; 9 MMA issuer.
+// Shared memory (D = 128): Q^ 32K, K^ x2 64K, V^ x2 64K, P 32K, P^ 32K.
+#include "attn_common.cuh"
+
+namespace attnqat {
+namespace {
+
+constexpr int kThreadsFwd = 10 * 32;
+constexpr int kWarpTmaF = 8;
+constexpr int kWarpMmaF = 9;
+
+template <int D>
+struct FwdLayout {
+  static constexpr uint32_t kTile = 128 * D * 2;
+  static constexpr uint32_t kQ = 0;
+  static constexpr uint32_t kK0 = kQ + kTile;
+  static constexpr uint32_t kK1 = kK0 + kTile;
+  static constexpr uint32_t kV0 = kK1 + kTile;
+  static constexpr uint32_t kV1 = kV0 + kTile;
+  static constexpr uint32_t kP = kV1 + kTile;            // 128 x 128 BF16
+  static constexpr uint32_t kPH = kP + 2 * kBlockBytes;  // 128 x 128 BF16
+  static constexpr uint32_t kML = kPH + 2 * kBlockBytes; // 128 rows x (m, l) of half 1, then 128 lse2
+  static constexpr uint32_t kBar = kML + 1536;
+  static constexpr uint32_t kBytes = kBar + 256;
+  static constexpr uint32_t kAlloc = kBytes + 1024;
+  static constexpr uint32_t kColS0 = 0;
+  static constexpr uint32_t kColOP = 256;
+  static constexpr uint32_t kColO = 256 + D;
+};
+
+struct FwdBars {
+  uint64_t q_full;
+  uint64_t k_full[2];
+  uint64_t k_empty[2];
+  uint64_t v_full[2];
+  uint64_t v_empty[2];
+  uint64_t s_full[2];
+  uint64_t s_free[2];
+  uint64_t p_ready;
+  uint64_t pv_done;
+  uint64_t ml_ready;
+  uint64_t lse_ready;
+  uint64_t drain;
+  uint32_t tmem_base;
+  uint32_t abort_flag;
+};
+
+struct FwdArgs {
+  bf16* o;
+  bf16* o_hp;
+  float* lse;
+  int Sq, Sk;
+  int n_qtiles, n_ktiles;
+  int causal;
+  float c2;   // scale * log2(e)
+  uint32_t* err;
+  uint64_t timeout_ns;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreadsFwd, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
+  using L = FwdLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  FwdBars& B = *reinterpret_cast<FwdBars*>(smem + L::kBar);
+  float* ml = reinterpret_cast<float*>(smem + L::kML);
+
+  const int warp = warp_id();
+  const int lane = lane_id();
+  // Causal tiles have i + 1 key tiles: launch the longest first.
+  const int i = a.causal ? (a.n_qtiles - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+  const int bh = blockIdx.y;
+  const int nk = a.causal ? i + 1 : a.n_ktiles;
+  const int nt = 2 * nk;                     // pass 1: t < nk; pass 2: t >= nk
+
+  if (threadIdx.x == 0) {
+    B.abort_flag = 0;
+    mbar_init(&B.q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&B.k_full[s], 1), mbar_init(&B.k_empty[s], 1);
+      mbar_init(&B.v_full[s], 1), mbar_init(&B.v_empty[s], 1);
+      mbar_init(&B.s_full[s], 1), mbar_init(&B.s_free[s], 256);
+    }
+    mbar_init(&B.p_ready, 256);
+    mbar_init(&B.pv_done, 1);
+    mbar_init(&B.ml_ready, 128);
+    mbar_init(&B.lse_ready, 128);
+    mbar_init(&B.drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == kWarpMmaF) {
+    tmem_alloc(&B.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = B.tmem_base;
+  const WaitCtl ctl{&B.abort_flag, a.err, a.timeout_ns};
+
+  if (warp == kWarpTmaF) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q), tma_prefetch_desc(&tm_k), tma_prefetch_desc(&tm_v);
+      int k_uses[2] = {0, 0}, v_uses[2] = {0, 0};
+      mbar_arrive_expect_tx(&B.q_full, L::kTile);
+      for (int b = 0; b < D / 64; ++b)
+        tma_load_3d(smem + L::kQ + b * kBlockBytes, &tm_q, &B.q_full, b * 64, i * 128, bh);
+      for (int t = 0; t < nt; ++t) {
+        const int jt = t < nk ? t : t - nk;
+        const int s = t & 1;
+        if (t >= 2 && !mbar_wait(&B.k_empty[s], ((t >> 1) - 1) & 1, ctl)) break;
+        mbar_arrive_expect_tx(&B.k_full[s], L::kTile);
+        for (int b = 0; b < D / 64; ++b)
+          tma_load_3d(smem + (s ? L::kK1 : L::kK0) + b * kBlockBytes, &tm_k, &B.k_full[s], b * 64, jt * 128, bh);
+        ++k_uses[s];
+        if (t >= nk) {
+          const int tv = t - nk, sv = tv & 1;
+          if (tv >= 2 && !mbar_wait(&B.v_empty[sv], ((tv >> 1) - 1) & 1, ctl)) break;
+          mbar_arrive_expect_tx(&B.v_full[sv], L::kTile);
+          for (int b = 0; b < D / 64; ++b)
+            tma_load_3d(smem + (sv ? L::kV1 : L::kV0) + b * kBlockBytes, &tm_v, &B.v_full[sv], b * 64, jt * 128, bh);
+          ++v_uses[sv];
+        }
+      }
+      mbar_wait_drain(&B.q_full, 0, ctl);
+      for (int s = 0; s < 2; ++s) {
+        if (k_uses[s]) mbar_wait_drain(&B.k_full[s], (k_uses[s] - 1) & 1, ctl);
+        if (v_uses[s]) mbar_wait_drain(&B.v_full[s], (v_uses[s] - 1) & 1, ctl);
+      }
+    }
+  } else if (warp == kWarpMmaF) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t kIdO = idesc_bf16(128, D, false, true);
+      auto issue_s = [&](int t) -> bool {
+        const int s = t & 1;
+        if (!mbar_wait(&B.k_full[s], (t >> 1) & 1, ctl)) return false;
+        if (t >= 2 && !mbar_wait(&B.s_free[s], ((t >> 1) - 1) & 1, ctl)) return false;
+        tc_fence_after();
+        const uint32_t kb = s ? L::kK1 : L::kK0;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t o = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
+          umma_bf16(tmem + L::kColS0 + s * 128, sdesc_sw128(sbase + L::kQ + o, 16, 1024),
+                    sdesc_sw128(sbase + kb + o, 16, 1024), kIdS, kk > 0);
+        }
+        umma_commit(&B.s_full[s]);
+        umma_commit(&B.k_empty[s]);
+        return true;
+      };
+      // O (+)= A[128 q x 128 keys] V^[128 keys x D]: A K-major, V^ MN-major.
+      auto mma_pv = [&](uint32_t a_off, uint32_t v_off, uint32_t col, bool acc) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t oa = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
+          umma_bf16(tmem + col, sdesc_sw128(sbase + a_off + oa, 16, 1024),
+                    sdesc_sw128(sbase + v_off + kk * 2048, kBlockBytes, 1024), kIdO, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(&B.q_full, 0, ctl) && issue_s(0);
+      for (int t = 0; ok && t < nt; ++t) {
+        if (t + 1 < nt && !issue_s(t + 1)) break;
+        if (t >= nk) {
+          const int tv = t - nk, sv = tv & 1;
+          if (!mbar_wait(&B.v_full[sv], (tv >> 1) & 1, ctl)) break;
+          if (!mbar_wait(&B.p_ready, tv & 1, ctl)) break;
+          tc_fence_after();
+          const uint32_t vb = sv ? L::kV1 : L::kV0;
+          mma_pv(L::kP, vb, L::kColOP, tv > 0);
+          mma_pv(L::kPH, vb, L::kColO, tv > 0);
+          umma_commit(&B.pv_done);
+          umma_commit(&B.v_empty[sv]);
+        }
+      }
+      umma_commit(&B.drain);
+      mbar_wait_drain(&B.drain, 0, ctl);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax (warps 0-7)
+    const uint32_t quarter = warp & 3, half = warp >> 2;
+    const uint32_t r = quarter * 32 + lane;
+    const uint32_t lane_off = (quarter * 32u) << 16;
+    const int qrow = i * 128 + r;
+    const int kend = a.causal ? min(a.Sk, qrow + 1) : a.Sk;
+    bool ok = true;
+
+    // pass 1: running max and sum of exp2(S * c2) over this thread's key columns
+    float m = -INFINITY, l = 0.0f;
+    for (int t = 0; t < nk; ++t) {
+      const int s = t & 1;
+      const int valid = kend - (t * 128 + static_cast<int>(half) * 64);
+      if (!warp_wait(&B.s_full[s], (t >> 1) & 1, ctl)) { ok = false; break; }
+      tc_fence_after();
+      float x[64];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + L::kColS0 + s * 128 + half * 64 + c * 32, v);
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+          x[c * 32 + k] = (c * 32 + k < valid) ? __uint_as_float(v[k]) * a.c2 : -INFINITY;
+      }
+      tc_fence_before();
+      mbar_arrive(&B.s_free[s]);
+      float mx = m;
+#pragma unroll
+      for (int k = 0; k < 64; ++k) mx = fmaxf(mx, x[k]);
+      if (mx == -INFINITY) continue;
+      float sum = 0.0f;
+#pragma unroll
+      for (int k = 0; k < 64; ++k) sum += ex2(x[k] - mx);
+      l = l * ex2(m - mx) + sum;
+      m = mx;
+    }
+    // Combine the two column halves of each row: half 1 hands (m, l) to half
+    // 0, which forms lse2 = log2 sum 2^(S*c2), stores LSE and hands lse2 back.
+    float lse2 = 0.0f;
+    float* lse_s = ml + 256;
+    if (ok && half == 1) {
+      ml[r * 2] = m;
+      ml[r * 2 + 1] = l;
+      mbar_arrive(&B.ml_ready);
+      if (warp_wait(&B.lse_ready, 0, ctl))
+        lse2 = lse_s[r];
+      else
+        ok = false;
+    } else if (ok) {
+      if (warp_wait(&B.ml_ready, 0, ctl)) {
+        const float m1 = ml[r * 2], l1 = ml[r * 2 + 1];
+        const float M = fmaxf(m, m1);
+        const float Lsum = (m == -INFINITY ? 0.0f : l * ex2(m - M)) + (m1 == -INFINITY ? 0.0f : l1 * ex2(m1 - M));
+        lse2 = M + lg2(Lsum);
+        lse_s[r] = lse2;
+        mbar_arrive(&B.lse_ready);
+        if (qrow < a.Sq) a.lse[(size_t)bh * a.Sq + qrow] = lse2 * kLn2;
+      } else {
+        ok = false;
+      }
+    }
+
+    // pass 2: P = exp2(S * c2 - lse2), P^ = fake_nvfp4(P); hand both to the MMA warp
+    const uint32_t p_block = sbase + L::kP + half * kBlockBytes;
+    const uint32_t ph_block = sbase + L::kPH + half * kBlockBytes;
+    for (int t = nk; ok && t < nt; ++t) {
+      const int s = t & 1, tv = t - nk;
+      const int valid = kend - (tv * 128 + static_cast<int>(half) * 64);
+      if (!warp_wait(&B.s_full[s], (t >> 1) & 1, ctl)) { ok = false; break; }
+      tc_fence_after();
+      float P[64];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + L::kColS0 + s * 128 + half * 64 + c * 32, v);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float p = ex2(fmaf(__uint_as_float(v[k]), a.c2, -lse2));
+          P[c * 32 + k] = (c * 32 + k < valid) ? p : 0.0f;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&B.s_free[s]);
+      uint32_t pw[32], phw[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) pw[k] = pack_bf16x2(P[2 * k], P[2 * k + 1]);
+#pragma unroll
+      for (int g = 0; g < 4; ++g) quant_pack16(P + 16 * g, phw + 8 * g);
+      if (tv > 0 && !warp_wait(&B.pv_done, (tv - 1) & 1, ctl)) { ok = false; break; }
+      store_row64(p_block, r, pw);
+      store_row64(ph_block, r, phw);
+      fence_proxy_async_smem();
+      mbar_arrive(&B.p_ready);
+    }
+    // epilogue: O' and O rows, columns [half*D/2, +D/2)
+    if (ok && warp_wait(&B.pv_done, (nk - 1) & 1, ctl)) {
+      tc_fence_after();
+      const size_t row = (size_t)bh * a.Sq + qrow;
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        const uint32_t col = half * (D / 2) + c * 32;
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + L::kColOP + col, v);
+        if (qrow < a.Sq) store_row32_bf16(a.o_hp + row * D + col, v, 1.0f);
+        tmem_ld32(tmem + lane_off + L::kColO + col, v);
+        if (qrow < a.Sq) store_row32_bf16(a.o + row * D + col, v, 1.0f);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMmaF) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const Problem& p, const bf16* qh, const bf16* kh, const bf16* vh, bf16* o, bf16* o_hp,
+                       float* lse, uint32_t* err, cudaStream_t st) {
+  CUtensorMap tq, tk, tv;
+  const uint64_t bh = p.bh();
+  if (!make_tile_map(&tq, qh, false, p.D, p.Sq, bh, 64, 128) || !make_tile_map(&tk, kh, false, p.D, p.Sk, bh, 64, 128) ||
+      !make_tile_map(&tv, vh, false, p.D, p.Sk, bh, 64, 128))
+    return cudaErrorInvalidValue;
+  FwdArgs a;
+  a.o = o, a.o_hp = o_hp, a.lse = lse;
+  a.Sq = static_cast<int>(p.Sq), a.Sk = static_cast<int>(p.Sk);
+  a.n_qtiles = static_cast<int>((p.Sq + kBlockM - 1) / kBlockM);
+  a.n_ktiles = static_cast<int>((p.Sk + kBlockN - 1) / kBlockN);
+  a.causal = p.causal ? 1 : 0;
+  a.c2 = p.scale * kLog2e;
+  a.err = err, a.timeout_ns = kWaitTimeoutNs;
+  const dim3 grid(static_cast<unsigned>(a.n_qtiles), static_cast<unsigned>(bh));
+  if (p.D == 128) {
+    cudaError_t e = set_smem(reinterpret_cast<const void*>(&fwd_kernel<128>), FwdLayout<128>::kAlloc);
+    if (e != cudaSuccess) return e;
+    fwd_kernel<128><<<grid, kThreadsFwd, FwdLayout<128>::kAlloc, st>>>(tq, tk, tv, a);
+  } else {
+    cudaError_t e = set_smem(reinterpret_cast<const void*>(&fwd_kernel<64>), FwdLayout<64>::kAlloc);
+    if (e != cudaSuccess) return e;
+    fwd_kernel<64><<<grid, kThreadsFwd, FwdLayout<64>::kAlloc, st>>>(tq, tk, tv, a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace attnqat

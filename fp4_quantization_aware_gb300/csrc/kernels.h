@@ -1,0 +1,49 @@
+// Host-side launchers of the CUDA kernels (internal to libattnqat).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace attnqat {
+
+using bf16 = __nv_bfloat16;
+
+struct Problem {
+  int64_t B, H, Sq, Sk, D;
+  bool causal;
+  float scale;
+  int64_t bh() const { return B * H; }
+};
+
+// Kernel tile sizes: 128 query rows x 128 keys per step in both directions.
+constexpr int kBlockM = 128;
+constexpr int kBlockN = 128;
+
+// Wait limit of the attention kernels' barrier waits.
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+
+cudaError_t launch_fake_bf16(const bf16* x, bf16* y, int64_t rows, int64_t cols, cudaStream_t st);
+cudaError_t launch_fake_f32(const float* x, float* y, int64_t rows, int64_t cols, cudaStream_t st);
+
+// Q^, K^, V^ (and, when o_hp != nullptr, delta = rowsum(O' * dO) and a zeroed
+// FP32 dQ accumulator).
+cudaError_t launch_prep(const Problem& p, const bf16* q, const bf16* k, const bf16* v, const bf16* o_hp,
+                        const bf16* dout, bf16* qh, bf16* kh, bf16* vh, float* delta, float* dq_acc,
+                        cudaStream_t st);
+
+cudaError_t launch_dq_convert(const Problem& p, const float* dq_acc, bf16* dq, cudaStream_t st);
+
+cudaError_t launch_fwd(const Problem& p, const bf16* qh, const bf16* kh, const bf16* vh, bf16* o, bf16* o_hp,
+                       float* lse, uint32_t* err, cudaStream_t st);
+
+cudaError_t launch_bwd(const Problem& p, const bf16* qh, const bf16* kh, const bf16* vh, const bf16* dout,
+                       const float* lse, const float* delta, float* dq_acc, bf16* dk, bf16* dv, uint32_t* err,
+                       cudaStream_t st);
+
+cudaError_t launch_wait_timeout(uint32_t* err, uint64_t timeout_ns, cudaStream_t st);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against libcuda). Returns nullptr if the driver does not provide it.
+void* tensor_map_encoder();
+
+}  // namespace attnqat

@@ -1,0 +1,204 @@
+// HBM-bound kernels of the Attn-QAT path:
+//  - fake_nvfp4 of BF16 and FP32 matrices (groups of 16 along rows),
+//  - the fused preprocess: Q^, K^, V^ along D ("NVFP4 Attention QAT Backward",
+//    Overview: fused Q fake-quantization/delta preprocessing and K/V
+//    fake-quantization), delta = rowsum(O' * dO), and zeroing of the FP32 dQ
+//    accumulator that the backward kernel adds into,
+//  - the dQ FP32 -> BF16 conversion,
+//  - the bounded-wait self-test.
+// One thread owns one 16-value group (32 bytes of BF16): a warp moves 1 KiB
+// contiguous per access, and the D/16 threads of a row reduce delta with
+// shuffles.
+#include "kernels.h"
+#include "nvfp4.cuh"
+
+namespace attnqat {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ void unpack8(const uint4& u, float* f) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint4 pack8(const float* f) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                    pack_bf16x2(f[6], f[7]));
+}
+
+__device__ __forceinline__ void load16(const bf16* p, float (&f)[16]) {
+  const uint4* v = reinterpret_cast<const uint4*>(p);
+  unpack8(__ldg(v), f);
+  unpack8(__ldg(v + 1), f + 8);
+}
+
+__device__ __forceinline__ void store16(bf16* p, const float (&f)[16]) {
+  uint4* v = reinterpret_cast<uint4*>(p);
+  v[0] = pack8(f);
+  v[1] = pack8(f + 8);
+}
+
+// ------------------------------------------------------------ generic quantizers
+__global__ void __launch_bounds__(kThreads) fake_bf16_kernel(const bf16* x, bf16* y,
+                                                             int64_t rows, int64_t cols) {
+  const int64_t gpr = (cols + 15) / 16;
+  const int64_t g = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+  if (g >= rows * gpr) return;
+  const int64_t r = g / gpr, c0 = (g % gpr) * 16;
+  const int64_t base = r * cols + c0;
+  float f[16];
+  if ((cols & 15) == 0) {
+    load16(x + base, f);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) f[i] = (c0 + i < cols) ? __bfloat162float(x[base + i]) : 0.0f;
+  }
+  fake_nvfp4_16(f);
+  if ((cols & 15) == 0) {
+    store16(y + base, f);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (c0 + i < cols) y[base + i] = __float2bfloat16_rn(f[i]);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) fake_f32_kernel(const float* x, float* y,
+                                                            int64_t rows, int64_t cols) {
+  const int64_t gpr = (cols + 15) / 16;
+  const int64_t g = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+  if (g >= rows * gpr) return;
+  const int64_t r = g / gpr, c0 = (g % gpr) * 16;
+  const int64_t base = r * cols + c0;
+  float f[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) f[i] = (c0 + i < cols) ? x[base + i] : 0.0f;
+  fake_nvfp4_16(f);
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    if (c0 + i < cols) y[base + i] = f[i];
+}
+
+// ------------------------------------------------------------ fused preprocess
+struct PrepArgs {
+  const bf16* src[3];   // q, k, v
+  bf16* dst[3];         // q^, k^, v^
+  int64_t groups[3];    // 16-groups per tensor
+  const bf16* o_hp;     // null: forward (no delta, no dQ accumulator)
+  const bf16* dout;
+  float* delta;
+  float* dq_acc;
+};
+
+// blockIdx.y selects the tensor (0: Q with delta, 1: K, 2: V).
+template <int D>
+__global__ void __launch_bounds__(kThreads) prep_kernel(PrepArgs a) {
+  constexpr int kGroupsPerRow = D / 16;
+  const int t = blockIdx.y;
+  const int64_t g = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+  const bool live = g < a.groups[t];
+  if (blockIdx.x * static_cast<int64_t>(kThreads) >= a.groups[t]) return;   // whole block out of range
+  float f[16];
+  if (live) {
+    load16(a.src[t] + g * 16, f);
+    fake_nvfp4_16(f);
+    store16(a.dst[t] + g * 16, f);
+  }
+  if (t != 0 || a.o_hp == nullptr) return;
+  // delta = rowsum(O' * dO); every lane of the warp takes part in the shuffles.
+  float part = 0.0f;
+  if (live) {
+    float o[16], d[16];
+    load16(a.o_hp + g * 16, o);
+    load16(a.dout + g * 16, d);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) part = fmaf(o[i], d[i], part);
+    float4* z = reinterpret_cast<float4*>(a.dq_acc + g * 16);
+    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[0] = zero, z[1] = zero, z[2] = zero, z[3] = zero;
+  }
+#pragma unroll
+  for (int off = 1; off < kGroupsPerRow; off <<= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+  if (live && (g % kGroupsPerRow) == 0) a.delta[g / kGroupsPerRow] = part;
+}
+
+__global__ void __launch_bounds__(kThreads) dq_convert_kernel(const float4* __restrict__ acc, uint2* __restrict__ dq,
+                                                              int64_t n4) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+  if (i >= n4) return;
+  const float4 v = acc[i];
+  dq[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+}
+
+// One CTA waits on a barrier that nothing arrives at; the bounded wait gives
+// up after timeout_ns, records the error and the kernel returns.
+__global__ void wait_timeout_kernel(uint32_t* err, uint64_t timeout_ns) {
+  __shared__ uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    WaitCtl c{&abort_flag, err, timeout_ns};
+    (void)mbar_wait(&bar, 0, c);
+  }
+  __syncthreads();
+}
+
+inline unsigned blocks_for(int64_t n) { return static_cast<unsigned>((n + kThreads - 1) / kThreads); }
+
+}  // namespace
+
+cudaError_t launch_fake_bf16(const bf16* x, bf16* y, int64_t rows, int64_t cols, cudaStream_t st) {
+  const int64_t n = rows * ((cols + 15) / 16);
+  if (n == 0) return cudaSuccess;
+  fake_bf16_kernel<<<blocks_for(n), kThreads, 0, st>>>(x, y, rows, cols);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fake_f32(const float* x, float* y, int64_t rows, int64_t cols, cudaStream_t st) {
+  const int64_t n = rows * ((cols + 15) / 16);
+  if (n == 0) return cudaSuccess;
+  fake_f32_kernel<<<blocks_for(n), kThreads, 0, st>>>(x, y, rows, cols);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prep(const Problem& p, const bf16* q, const bf16* k, const bf16* v, const bf16* o_hp,
+                        const bf16* dout, bf16* qh, bf16* kh, bf16* vh, float* delta, float* dq_acc,
+                        cudaStream_t st) {
+  PrepArgs a;
+  a.src[0] = q, a.src[1] = k, a.src[2] = v;
+  a.dst[0] = qh, a.dst[1] = kh, a.dst[2] = vh;
+  a.groups[0] = p.bh() * p.Sq * (p.D / 16);
+  a.groups[1] = a.groups[2] = p.bh() * p.Sk * (p.D / 16);
+  a.o_hp = o_hp, a.dout = dout, a.delta = delta, a.dq_acc = dq_acc;
+  const int64_t most = a.groups[0] > a.groups[1] ? a.groups[0] : a.groups[1];
+  dim3 grid(blocks_for(most), 3);
+  if (p.D == 128)
+    prep_kernel<128><<<grid, kThreads, 0, st>>>(a);
+  else
+    prep_kernel<64><<<grid, kThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dq_convert(const Problem& p, const float* dq_acc, bf16* dq, cudaStream_t st) {
+  const int64_t n4 = p.bh() * p.Sq * p.D / 4;
+  dq_convert_kernel<<<blocks_for(n4), kThreads, 0, st>>>(reinterpret_cast<const float4*>(dq_acc),
+                                                         reinterpret_cast<uint2*>(dq), n4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_timeout(uint32_t* err, uint64_t timeout_ns, cudaStream_t st) {
+  wait_timeout_kernel<<<1, 32, 0, st>>>(err, timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace attnqat

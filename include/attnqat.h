@@ -1,0 +1,156 @@
+/*
+ * attnqat: Attn-QAT (scaled dot-product attention trained with NVFP4 fake
+ * quantization) for GB300 (sm_103a) behind a C ABI.
+ *
+ * The method ("NVFP4 Attention QAT Backward", cuDNN frontend docs, Overview;
+ * "Attn-QAT: 4-Bit Attention With Quantization-Aware Training", Method):
+ *
+ *   Q^, K^, V^ = fake_nvfp4(Q), fake_nvfp4(K), fake_nvfp4(V)  (16-groups along D)
+ *   P   = softmax(softmax_scale * Q^ K^T)                     (FP32)
+ *   O   = fake_nvfp4(P) V^                                    (16-groups of keys)
+ *   O'  = P V^                       (high-precision auxiliary output, "Fix 1")
+ *   LSE = natural-log log-sum-exp of the scaled logits
+ *   dS  = P * (dO V^T - rowsum(O' * dO))
+ *   dQ  = softmax_scale * dS K^,  dK = softmax_scale * dS^T Q^
+ *   dV  = fake_nvfp4(P)^T dO         (P recomputed from LSE, "Fix 2")
+ *
+ * fake_nvfp4 of a group of 16 values: s = RNE_E4M3(amax / 6) with IEEE
+ * division (saturating to 448); y = RNE_E2M1(x / s) * s with IEEE division
+ * (saturating to 6); y = +-0 when s == 0.
+ *
+ * Conventions shared by every entry point:
+ *  - Tensors are device pointers to contiguous BHSD storage: Q, O, O', dO, dQ
+ *    are (B, H, Sq, D); K, V, dK, dV are (B, H, Sk, D); LSE is (B, H, Sq).
+ *    Activations are BF16 (passed as void*), LSE is FP32. Every pointer must
+ *    be 16-byte aligned and all of them must live on the current device.
+ *  - The caller owns every buffer. No entry point allocates device memory;
+ *    scratch space comes from the caller's workspace.
+ *  - `stream` is a cudaStream_t (NULL is the legacy default stream). All work
+ *    is enqueued on it in order; nothing synchronizes the host.
+ *  - Argument, shape, alignment and workspace checks run on the host before
+ *    any launch and return an error without enqueuing anything.
+ *  - Every wait inside a kernel is bounded. A wait that runs out of time makes
+ *    the kernel return early and records ATTNQAT_ERR_TIMEOUT in a device
+ *    error word, read by attnqat_device_status().
+ */
+#ifndef ATTNQAT_H_
+#define ATTNQAT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum attnqat_status {
+  ATTNQAT_OK = 0,
+  ATTNQAT_ERR_INVALID_ARG = 1,   /* null pointer, negative size, bad scale */
+  ATTNQAT_ERR_UNSUPPORTED = 2,   /* D not in {64, 128}; causal with Sq != Sk */
+  ATTNQAT_ERR_MISALIGNED = 3,    /* a pointer is not 16-byte aligned */
+  ATTNQAT_ERR_WORKSPACE = 4,     /* workspace null, misaligned or too small */
+  ATTNQAT_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed */
+  ATTNQAT_ERR_TIMEOUT = 6        /* a bounded device wait ran out of time */
+} attnqat_status;
+
+/* One attention problem. MHA only (equal query and key/value head counts,
+ * cuDNN page "Current support and limitations"). is_causal drops keys j > i
+ * and needs Sq == Sk; softmax_scale must be finite and > 0 (the pages'
+ * default is 1/sqrt(128)) and must be the same in the forward and backward. */
+typedef struct attnqat_problem {
+  int64_t B, H, Sq, Sk, D;
+  int32_t is_causal;
+  float softmax_scale;
+} attnqat_problem;
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int attnqat_version(void);
+
+/* A static, human-readable name of a status code. */
+const char* attnqat_status_string(int status);
+
+/* Detail of the last error returned on the calling thread (empty if none). */
+const char* attnqat_last_error_message(void);
+
+/* Host-only check of a problem: ATTNQAT_OK if the kernels support it.
+ * B, H >= 1; Sq, Sk >= 1 and below 2^31; D in {64, 128}; causal needs
+ * Sq == Sk. Launches nothing and needs no GPU. */
+attnqat_status attnqat_check_support(const attnqat_problem* p);
+
+/* Workspace bytes for attnqat_fwd / attnqat_bwd (0 if the problem is not
+ * supported). Forward: Q^, K^, V^ (BF16). Backward: Q^, K^, V^, delta (FP32,
+ * B*H*Sq) and an FP32 dQ accumulator (B*H*Sq*D). */
+size_t attnqat_fwd_workspace_bytes(const attnqat_problem* p);
+size_t attnqat_bwd_workspace_bytes(const attnqat_problem* p);
+
+/* fake_nvfp4 of a row-major (rows, cols) BF16 matrix, groups of 16 along the
+ * contiguous axis starting at column 0 (a ragged last group is padded with
+ * zeros). x and y are device pointers (16-byte aligned) and may alias.
+ * Source: cuDNN page, Overview (the Q/K/V quantizer). */
+attnqat_status attnqat_fake_nvfp4(const void* x_bf16, void* y_bf16, int64_t rows, int64_t cols, void* stream);
+
+/* The same quantizer on FP32 input and output: the exact device routine the
+ * attention kernels apply to the probabilities P (groups of 16 keys). */
+attnqat_status attnqat_fake_nvfp4_f32(const float* x, float* y, int64_t rows, int64_t cols, void* stream);
+
+/* Forward. Inputs q, k, v (BF16). Outputs o = fake_nvfp4(P) V^, o_hp = P V^
+ * (both BF16, shape of q) and lse (FP32, natural log). Needs a workspace of
+ * attnqat_fwd_workspace_bytes(p) bytes, 256-byte aligned. Equivalent to
+ * attnqat_quantize_qkv followed by attnqat_fwd_main. */
+attnqat_status attnqat_fwd(const attnqat_problem* p, const void* q, const void* k, const void* v, void* o,
+                           void* o_hp, float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Backward. Inputs dO, q, k, v, o_hp (the matching forward's O' = P V^, not
+ * O; any other auxiliary gives wrong gradients) and lse (the matching
+ * forward's FP32 natural-log LSE). Outputs dq, dk, dv (BF16). Needs a
+ * workspace of attnqat_bwd_workspace_bytes(p) bytes, 256-byte aligned.
+ * Equivalent to attnqat_bwd_preprocess, attnqat_bwd_main, attnqat_bwd_dq_convert. */
+attnqat_status attnqat_bwd(const attnqat_problem* p, const void* dout, const void* q, const void* k,
+                           const void* v, const void* o_hp, const float* lse, void* dq, void* dk, void* dv,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---- the steps of attnqat_fwd / attnqat_bwd, for callers that time or
+ * schedule them separately. Each takes the same workspace. ---- */
+
+/* Forward step 1: Q^, K^, V^ into the workspace (HBM-bound). */
+attnqat_status attnqat_quantize_qkv(const attnqat_problem* p, const void* q, const void* k, const void* v,
+                                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* Forward step 2: the attention kernel on the workspace's Q^, K^, V^ (pass 1:
+ * LSE; pass 2: P, fake_nvfp4(P), O' and O). */
+attnqat_status attnqat_fwd_main(const attnqat_problem* p, void* o, void* o_hp, float* lse, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/* Backward step 1: Q^, K^, V^, delta = rowsum(O' * dO) into the workspace and
+ * the FP32 dQ accumulator zeroed (one HBM-bound kernel). */
+attnqat_status attnqat_bwd_preprocess(const attnqat_problem* p, const void* dout, const void* q, const void* k,
+                                      const void* v, const void* o_hp, void* workspace, size_t workspace_bytes,
+                                      void* stream);
+
+/* Backward step 2: the dK/dV kernel (one CTA per 128-key tile), which also
+ * adds every tile's dQ contribution into the workspace's FP32 accumulator. */
+attnqat_status attnqat_bwd_main(const attnqat_problem* p, const void* dout, const float* lse, void* dk, void* dv,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/* Backward step 3: dQ (BF16) from the FP32 accumulator. */
+attnqat_status attnqat_bwd_dq_convert(const attnqat_problem* p, void* dq, void* workspace, size_t workspace_bytes,
+                                      void* stream);
+
+/* ---- device status ---- */
+
+/* Synchronizes the current device, then returns ATTNQAT_OK or the first
+ * device-side error recorded since the last clear (ATTNQAT_ERR_TIMEOUT), or
+ * ATTNQAT_ERR_CUDA if the synchronization failed. clear != 0 resets it. */
+attnqat_status attnqat_device_status(int clear);
+
+/* Launches one CTA that waits on a barrier that nothing arrives at, with a
+ * limit of timeout_ns nanoseconds; it then records ATTNQAT_ERR_TIMEOUT in the
+ * device error word and returns. Exercises the bounded-wait path without
+ * faulting or hanging the GPU. */
+attnqat_status attnqat_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTNQAT_H_ */

