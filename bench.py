@@ -1,0 +1,336 @@
+"""Attn-QAT benchmark: backward (and forward) TFLOP/s on one GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c2] [--impl ours|reference]
+
+A step is one pass of the whole path over one batch of synthetic input:
+quantize Q/K/V + forward (O, O', LSE), then preprocess + backward (dQ, dK,
+dV) on that forward's O' and LSE. The L2 cache is flushed (256 MiB write)
+between steps, outside the timed kernels. FLOPs are nominal: forward
+4*B*H*Sq*Sk*D, backward 10*B*H*Sq*Sk*D, halved for causal.
+
+`value` is the backward TFLOP/s (CUDA events around the backward API calls);
+`roofline` reports the backward main kernel alone against the measured dense
+BF16 peak; `e2e` repeats the backward through the C ABI with pinned host
+buffers, host<->device copies inside the timed region; `cpu_baseline` times
+the float64 CPU oracle on whole heads of the same workload (about 10 s).
+
+With --gpus N (launched by torchrun) every rank runs the full workload on its
+own GPU (independent problems, no collective on the data path) and `value` is
+the sum over ranks divided by the slowest rank's time (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from fp4_quantization_aware_gb300 import synth  # noqa: E402
+
+PROFILE_JSON = os.path.join(ROOT, "profiles", "bwd_main_c2_counters.json")
+KERNEL_SOURCES = [os.path.join(ROOT, "fp4_quantization_aware_gb300", "csrc", f)
+                  for f in ("bwd.cu", "attn_common.cuh", "nvfp4.cuh", "ptx.cuh")]
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"bf16": d["bf16_tflops"], "bf16_sustained": d.get("bf16_tflops_sustained"), "hbm": d["hbm_gbs"],
+                "src": "measured"}
+    return {"bf16": 1900.0, "bf16_sustained": 1700.0, "hbm": 6800.0, "src": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- ours
+def run_ours(args, w, rank, world, local_rank):
+    import torch
+    from fp4_quantization_aware_gb300 import attnqat
+    import ctypes
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    lib = attnqat.load()
+    x = synth.inputs(w)
+    t = {n: torch.from_numpy(a).to(torch.bfloat16).to(dev) for n, a in x.items()}
+    p = attnqat.problem(w.B, w.H, w.Sq, w.Sk, w.D, w.causal, w.scale)
+    pp = ctypes.byref(p)
+    ws_f = attnqat.workspace(lib.attnqat_fwd_workspace_bytes(pp), dev)
+    ws_b = attnqat.workspace(lib.attnqat_bwd_workspace_bytes(pp), dev)
+    o, o_hp = torch.empty_like(t["q"]), torch.empty_like(t["q"])
+    lse = torch.empty(w.shape_q[:3], dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(t["q"]), torch.empty_like(t["k"]), torch.empty_like(t["v"])
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    P = lambda a: a.data_ptr()  # noqa: E731
+
+    def fwd():
+        attnqat.check(lib.attnqat_quantize_qkv(pp, P(t["q"]), P(t["k"]), P(t["v"]), P(ws_f), ws_f.numel(), sp), "q")
+        attnqat.check(lib.attnqat_fwd_main(pp, P(o), P(o_hp), P(lse), P(ws_f), ws_f.numel(), sp), "fwd")
+
+    def bwd(ev=None):
+        attnqat.check(lib.attnqat_bwd_preprocess(pp, P(t["do"]), P(t["q"]), P(t["k"]), P(t["v"]), P(o_hp),
+                                                 P(ws_b), ws_b.numel(), sp), "prep")
+        if ev:
+            ev[0].record(stream)
+        attnqat.check(lib.attnqat_bwd_main(pp, P(t["do"]), P(lse), P(dk), P(dv), P(ws_b), ws_b.numel(), sp), "bwd")
+        if ev:
+            ev[1].record(stream)
+        attnqat.check(lib.attnqat_bwd_dq_convert(pp, P(dq), P(ws_b), ws_b.numel(), sp), "dqc")
+
+    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    for _ in range(args.warmup):
+        flush.zero_()
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    evs = [(E(), E(), E(), E(), E()) for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clk:
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for e in evs:
+            flush.zero_()
+            e[0].record(stream)
+            fwd()
+            e[1].record(stream)
+            bwd(ev=(e[2], e[3]))
+            e[4].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    if world > 1:
+        torch.distributed.barrier()
+    fwd_ms = sum(e[0].elapsed_time(e[1]) for e in evs)
+    bwd_ms = sum(e[1].elapsed_time(e[4]) for e in evs)
+    main_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    step_ms = (fwd_ms + bwd_ms) / args.steps
+    launches = 5 * args.steps
+    assert attnqat.device_status() == 0, "a device wait timed out during the bench"
+
+    # end to end through the C ABI with pinned host buffers (backward step)
+    host_in = {n: t[n].cpu().pin_memory() for n in ("do", "q", "k", "v")}
+    host_in["o_hp"] = o_hp.cpu().pin_memory()
+    host_in["lse"] = lse.cpu().pin_memory()
+    dev_in = {n: torch.empty_like(v, device=dev) for n, v in host_in.items()}
+    host_out = [torch.empty_like(a, device="cpu").pin_memory() for a in (dq, dk, dv)]
+    e2e_evs = [(E(), E()) for _ in range(args.steps)]
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        if i >= args.warmup:
+            e2e_evs[i - args.warmup][0].record(stream)
+        for n in dev_in:
+            dev_in[n].copy_(host_in[n], non_blocking=True)
+        attnqat.check(lib.attnqat_bwd(pp, P(dev_in["do"]), P(dev_in["q"]), P(dev_in["k"]), P(dev_in["v"]),
+                                      P(dev_in["o_hp"]), P(dev_in["lse"]), P(dq), P(dk), P(dv), P(ws_b),
+                                      ws_b.numel(), sp), "bwd e2e")
+        for h, d in zip(host_out, (dq, dk, dv)):
+            h.copy_(d, non_blocking=True)
+        if i >= args.warmup:
+            e2e_evs[i - args.warmup][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_evs) / args.steps
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out)
+
+    res = {"fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "main_ms": main_ms, "step_ms": step_ms, "wall": wall,
+           "launches": launches, "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h, "clocks": clk.summary()}
+    if world > 1:
+        v = torch.tensor([bwd_ms, fwd_ms, step_ms, e2e_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(v, op=torch.distributed.ReduceOp.MAX)
+        res["bwd_ms"], res["fwd_ms"], res["step_ms"], res["e2e_ms"] = v.tolist()
+    return res
+
+
+# ---------------------------------------------------------------------------- CPU oracle
+def oracle_heads(w, heads):
+    """Time the float64 CPU oracle's forward and backward on the listed heads."""
+    import oracle
+    fwd_s = bwd_s = 0.0
+    for bh in heads:
+        x = synth.inputs(w, heads=[bh])
+        t0 = time.perf_counter()
+        o, o_hp, lse = oracle.attn_qat_fwd(x["q"], x["k"], x["v"], w.scale, w.causal)
+        t1 = time.perf_counter()
+        oracle.attn_qat_bwd(x["do"], x["q"], x["k"], x["v"], o_hp, lse, w.scale, w.causal)
+        fwd_s += t1 - t0
+        bwd_s += time.perf_counter() - t1
+    n = len(heads)
+    return {"fwd_s": fwd_s, "bwd_s": bwd_s, "fwd_flops": n * w.fwd_flops() / (w.B * w.H),
+            "bwd_flops": n * w.bwd_flops() / (w.B * w.H)}
+
+
+def cpu_baseline(w, budget_s: float = 10.0) -> dict:
+    """Oracle backward on whole heads, in order, until about budget_s of CPU work."""
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    r = oracle_heads(w, heads[:1])
+    n = max(1, min(len(heads), int(budget_s / max(r["fwd_s"] + r["bwd_s"], 1e-3))))
+    if n > 1:
+        r = oracle_heads(w, heads[:n])
+    return {"value": r["bwd_flops"] / r["bwd_s"] / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
+            "kind": "oracle", "sample": f"{n} of {len(heads)} heads of the workload, each full {w.Sq}x{w.Sk}: "
+            f"backward {r['bwd_s']:.2f} s, forward {r['fwd_s']:.2f} s, float64 NumPy (BLAS on all cores)"}
+
+
+def workload_config(w, l2) -> dict:
+    return {"workload": f"{w.name}: B={w.B} H={w.H} Sq={w.Sq} Sk={w.Sk} D={w.D} "
+            f"{'causal' if w.causal else 'non-causal'}, {w.structure} N(0,1) BF16, scale={w.scale:.6g}",
+            "B": w.B, "H": w.H, "Sq": w.Sq, "Sk": w.Sk, "D": w.D, "causal": w.causal, "l2": l2,
+            "step": "quantize+fwd, then preprocess+bwd+dQ convert"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="c2", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = synth.workload(args.workload)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    peaks = measured_peaks()
+    l2 = "flushed: 256 MiB write between steps"
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        t0 = time.perf_counter()
+        per = []
+        for _ in range(args.warmup + args.steps):
+            per.append(oracle_heads(w, [(0, 0)]))
+        per = per[args.warmup:]
+        bwd_s = sum(r["bwd_s"] for r in per)
+        val = sum(r["bwd_flops"] for r in per) / bwd_s / 1e12
+        sample = f"backward of head (b=0, h=0) of {w.B * w.H} per step (full {w.Sq}x{w.Sk}), float64 NumPy"
+        line = {"impl": "reference", "metric": "QAT attn bwd TFLOP/s (CPU float64 oracle)", "value": val,
+                "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1e3 * (bwd_s + sum(r["fwd_s"] for r in per)) / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": workload_config(w, l2),
+                "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                                 "sample": sample},
+                "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                "wall_s": time.perf_counter() - t0}
+        print(json.dumps(line))
+        return
+
+    import torch
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    r = run_ours(args, w, rank, world, local_rank)
+    if rank != 0:
+        torch.distributed.destroy_process_group()
+        return
+    flops_b, flops_f = w.bwd_flops(), w.fwd_flops()
+    value = world * flops_b * args.steps / (r["bwd_ms"] * 1e-3) / 1e12
+    main_ms = statistics.mean(r["main_ms"])
+    achieved = flops_b / (main_ms * 1e-3) / 1e12
+    traffic = None
+    if os.path.exists(PROFILE_JSON):
+        prof = json.load(open(PROFILE_JSON))
+        if prof.get("kernel_hash") == kernel_hash() and prof.get("workload") == w.name:
+            traffic = prof.get("dram_bytes_per_launch")
+    line = {
+        "metric": "QAT attn bwd TFLOP/s on 1 GB300 (fwd in fwd_tflops); % of dense BF16 peak in roofline",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": r["step_ms"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic", "config": workload_config(w, l2),
+        "fwd_tflops": world * flops_f * args.steps / (r["fwd_ms"] * 1e-3) / 1e12,
+        "step_tflops": world * (flops_f + flops_b) / (r["step_ms"] * 1e-3) / 1e12,
+        "bwd_ms": r["bwd_ms"] / args.steps, "fwd_ms": r["fwd_ms"] / args.steps,
+        "roofline": {"bound": "tensor", "kernel": "bwd_kernel<128> (attnqat_bwd_main)", "achieved": achieved,
+                     "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16"],
+                     "traffic": traffic, "launch_ms": main_ms,
+                     "peak_note": f"{peaks['src']} dense BF16 burst (cuBLAS); sustained {peaks['bf16_sustained']}"},
+        "e2e": {"value": world * flops_b / (r["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms": r["e2e_ms"],
+                "what": "attnqat_bwd with pinned host inputs (dO, Q, K, V, O', LSE) and outputs (dQ, dK, dV)"},
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
