@@ -127,6 +127,8 @@ T* at(void* ws, size_t off) {
 }  // namespace
 
 // ------------------------------------------------------------ shared host helpers
+void set_error_message(const char* msg) { snprintf(g_msg, sizeof(g_msg), "%s", msg); }
+
 void* tensor_map_encoder() {
   static void* fn = [] {
     void* f = nullptr;

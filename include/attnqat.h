@@ -136,6 +136,21 @@ attnqat_status attnqat_bwd_main(const attnqat_problem* p, const void* dout, cons
 attnqat_status attnqat_bwd_dq_convert(const attnqat_problem* p, void* dq, void* workspace, size_t workspace_bytes,
                                       void* stream);
 
+/* The backward for callers that cannot allocate device memory (code running
+ * where cudaMalloc is not allowed or not possible, or a fixed memory budget
+ * with no allocator hook). The paper has no counterpart: it exists only so
+ * that such callers need no workspace. It computes exactly what attnqat_bwd
+ * computes, with the scratch space in a 32 MiB static device array that the
+ * library declares; problems whose attnqat_bwd_workspace_bytes() exceed
+ * 32 MiB return ATTNQAT_ERR_WORKSPACE. It allocates nothing. Every GPU that
+ * loads the library holds the array until exit; all calls share it and it
+ * keeps the last call's contents, so calls that overlap on the GPU race.
+ * The first call on a device looks up the array's address (make it before any
+ * stream capture). */
+attnqat_status attnqat_bwd_noalloc(const attnqat_problem* p, const void* dout, const void* q, const void* k,
+                                   const void* v, const void* o_hp, const float* lse, void* dq, void* dk, void* dv,
+                                   void* stream);
+
 /* ---- device status ---- */
 
 /* Synchronizes the current device, then returns ATTNQAT_OK or the first

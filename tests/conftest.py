@@ -20,4 +20,6 @@ def lib():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     from fp4_quantization_aware_gb300 import attnqat
+    from fp4_quantization_aware_gb300 import build as builder
+    builder.build()
     return attnqat.load()
