@@ -56,6 +56,7 @@ SIGNATURES = {
     "attnqat_bwd_noalloc": (_S, [_PP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "attnqat_device_status": (_S, [ctypes.c_int]),
     "attnqat_selftest_wait_timeout": (_S, [ctypes.c_uint64, _P]),
+    "attnqat_selftest_quotient": (_S, [_P, _P]),
 }
 
 _lib = None

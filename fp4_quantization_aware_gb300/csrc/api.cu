@@ -315,6 +315,12 @@ attnqat_status attnqat_device_status(int clear) {
   return v == kDevTimeout ? fail(ATTNQAT_ERR_TIMEOUT, "a device wait ran out of time") : ATTNQAT_OK;
 }
 
+attnqat_status attnqat_selftest_quotient(unsigned long long* out, void* stream) {
+  ATTNQAT_TRY(check_ptrs({out}));
+  ATTNQAT_CUDA(launch_quotient_selftest(out, static_cast<cudaStream_t>(stream)), "selftest_quotient");
+  return ATTNQAT_OK;
+}
+
 attnqat_status attnqat_selftest_wait_timeout(uint64_t timeout_ns, void* stream) {
   attnqat_status st = ATTNQAT_OK;
   uint32_t* err = device_error_word(&st);

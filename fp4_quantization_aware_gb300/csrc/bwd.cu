@@ -12,11 +12,17 @@
 // diagonal; tiles past Sq/Sk are zero-filled by TMA and masked).
 //
 // Per query tile i (all MMAs tcgen05 kind::f16, BF16 in, FP32 in TMEM):
-//   S  = Q^_i K^T        (TMEM cols [0,128), lane = query row)
-//   dP = dO_i V^T        (cols [128,256))
+//   S  = Q^_i K^T        (128 columns, lane = query row)
+//   dP = dO_i V^T        (128 columns)
 //   dV += P^T dO_i       (cols [256,256+D), lane = key)   A = P^ from smem (MN-major)
 //   dK += dS^T Q^_i      (cols [256+D,256+2D))            A = dS from smem (MN-major)
-//   dQ_i = dS K^         (reuses the dP columns)          A = dS (K-major)
+//   dQ_i = dS K^         (over dP_i once it is read)      A = dS (K-major)
+// S, dP and dQ share two 128-column TMEM regions R0 = [0,128), R1 = [128,256).
+// Step `it` keeps dP and then dQ in R[(it+1)%2]; S of step it >= 1 is there
+// too (read before dP is written), S of step 0 is in R0. So dP of a step waits
+// only for the softmax warps to read that step's S, and S of the next step
+// goes into the region whose dQ was drained one step earlier: the dQ drain is
+// off the critical path.
 // Warp roles (14 warps):
 //   0-7  softmax: P = exp2(S*c - lse2), P^ = fake_nvfp4(P) -> smem, dS -> smem
 //        (warp w reads TMEM lanes 32*(w%4).., columns [64*(w/4), +64) of a tile)
@@ -50,11 +56,15 @@ struct BwdLayout {
   static constexpr uint32_t kBytes = kBar + 256;
   static constexpr uint32_t kAlloc = kBytes + 1024;      // room to align the base to 1024
   // TMEM columns
-  static constexpr uint32_t kColS = 0;
-  static constexpr uint32_t kColDP = 128;
+  static constexpr uint32_t kColR0 = 0;      // S / dP / dQ region 0
+  static constexpr uint32_t kColR1 = 128;    // S / dP / dQ region 1
   static constexpr uint32_t kColDV = 256;
   static constexpr uint32_t kColDK = 256 + D;
 };
+
+// TMEM column of the region holding S of step `it`, and of dP / dQ of step `it`.
+__device__ __forceinline__ uint32_t s_region(int it) { return it == 0 ? 0u : ((it + 1) & 1) * 128u; }
+__device__ __forceinline__ uint32_t dp_region(int it) { return ((it + 1) & 1) * 128u; }
 
 struct BwdBars {
   uint64_t kv_full;
@@ -65,7 +75,7 @@ struct BwdBars {
   uint64_t s_full;
   uint64_t s_free;
   uint64_t dp_full;
-  uint64_t dp_free;
+  uint64_t dq_free;
   uint64_t p_ready;
   uint64_t dv_done;
   uint64_t ds_ready;
@@ -117,7 +127,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     mbar_init(&B.s_full, 1);
     mbar_init(&B.s_free, 256);
     mbar_init(&B.dp_full, 1);
-    mbar_init(&B.dp_free, 128);
+    mbar_init(&B.dq_free, 128);
     mbar_init(&B.p_ready, 256);
     mbar_init(&B.dv_done, 1);
     mbar_init(&B.ds_ready, 256);
@@ -191,12 +201,12 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         }
       };
       // dQ[128 q x D] = dS[128 q x 128 keys] K^[128 keys x D]: A K-major, B MN-major.
-      auto mma_dq = [&]() {
+      auto mma_dq = [&](uint32_t col) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t oa = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
           const uint32_t ob = kk * 2048;
-          umma_bf16(tmem + L::kColDP, sdesc_sw128(sbase + L::kPS + oa, 16, 1024),
+          umma_bf16(tmem + col, sdesc_sw128(sbase + L::kPS + oa, 16, 1024),
                     sdesc_sw128(sbase + L::kK + ob, kBlockBytes, 1024), kIdQ, kk > 0);
         }
       };
@@ -204,15 +214,16 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       bool ok = mbar_wait(&B.kv_full, 0, ctl) && mbar_wait(&B.q_full[0], 0, ctl);
       if (ok) {
         tc_fence_after();
-        mma_nt(L::kQ0, L::kK, L::kColS);
+        mma_nt(L::kQ0, L::kK, s_region(0));
         umma_commit(&B.s_full);
       }
       for (int it = 0; ok && it < n_it; ++it) {
         const int s = it & 1;
         if (!mbar_wait(&B.do_full, it & 1, ctl)) break;
-        if (it >= 1 && !mbar_wait(&B.dp_free, (it - 1) & 1, ctl)) break;
+        // dP_it goes where S_it is (it >= 1): wait until the softmax warps read S_it.
+        if (it >= 1 && !mbar_wait(&B.s_free, it & 1, ctl)) break;
         tc_fence_after();
-        mma_nt(L::kDO, L::kV, L::kColDP);
+        mma_nt(L::kDO, L::kV, dp_region(it));
         umma_commit(&B.dp_full);
 
         if (!mbar_wait(&B.p_ready, it & 1, ctl)) break;
@@ -224,9 +235,10 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         if (it + 1 < n_it) {
           const int s1 = (it + 1) & 1;
           if (!mbar_wait(&B.q_full[s1], ((it + 1) >> 1) & 1, ctl)) break;
-          if (!mbar_wait(&B.s_free, it & 1, ctl)) break;
+          // S_{it+1} goes to region it%2: after S_0 is read (it == 0), else after dQ_{it-1} is drained.
+          if (it == 0 ? !mbar_wait(&B.s_free, 0, ctl) : !mbar_wait(&B.dq_free, (it - 1) & 1, ctl)) break;
           tc_fence_after();
-          mma_nt(s1 ? L::kQ1 : L::kQ0, L::kK, L::kColS);
+          mma_nt(s1 ? L::kQ1 : L::kQ0, L::kK, s_region(it + 1));
           umma_commit(&B.s_full);
         }
 
@@ -234,7 +246,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         tc_fence_after();
         mma_tn(L::kPS, s ? L::kQ1 : L::kQ0, L::kColDK, it > 0);
         umma_commit(&B.q_empty[s]);
-        mma_dq();
+        mma_dq(dp_region(it));
         umma_commit(&B.dq_full);
         umma_commit(&B.buf_free);
       }
@@ -250,28 +262,35 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     const uint32_t ps_block = sbase + L::kPS + half * kBlockBytes;
     const int key0 = j * 128 + half * 64;                    // first key of my 64 columns
     bool ok = true;
+    // LSE and delta of the row, loaded one step ahead (rows past Sq: P = 0).
+    auto row_stats = [&](int it, float& lse_out, float& dlt_out) {
+      const int row = (i_begin + it) * 128 + static_cast<int>(r);
+      lse_out = INFINITY, dlt_out = 0.0f;
+      if (it < n_it && row < a.Sq) {
+        lse_out = __ldg(a.lse + (size_t)bh * a.Sq + row);
+        dlt_out = __ldg(a.delta + (size_t)bh * a.Sq + row);
+      }
+    };
+    float lse_next, dlt_next;
+    row_stats(0, lse_next, dlt_next);
     for (int it = 0; it < n_it; ++it) {
       const int i = i_begin + it;
       const int qrow = i * 128 + r;
-      float lse2 = INFINITY, dlt = 0.0f;
-      if (qrow < a.Sq) {
-        lse2 = a.lse[(size_t)bh * a.Sq + qrow] * kLog2e;
-        dlt = a.delta[(size_t)bh * a.Sq + qrow];
-      }
+      const float lse2 = lse_next * kLog2e, dlt = dlt_next;
+      row_stats(it + 1, lse_next, dlt_next);
       const int kend = a.causal ? min(a.Sk, qrow + 1) : a.Sk;
       const int valid = kend - key0;                         // columns [0, valid) are live keys
 
       if (!warp_wait(&B.s_full, it & 1, ctl)) { ok = false; break; }
       tc_fence_after();
       float P[64];
+      {
+        uint32_t v[64];
+        tmem_ld64(tmem + lane_off + s_region(it) + half * 64, v);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_off + L::kColS + half * 64 + c * 32, v);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
+        for (int k = 0; k < 64; ++k) {
           const float p = ex2(fmaf(__uint_as_float(v[k]), a.c2, -lse2));
-          P[c * 32 + k] = (c * 32 + k < valid) ? p : 0.0f;
+          P[k] = (k < valid) ? p : 0.0f;
         }
       }
       tc_fence_before();
@@ -288,15 +307,14 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       if (!warp_wait(&B.dp_full, it & 1, ctl)) { ok = false; break; }
       tc_fence_after();
       uint32_t ds[32];
+      {
+        uint32_t v[64];
+        tmem_ld64(tmem + lane_off + dp_region(it) + half * 64, v);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_off + L::kColDP + half * 64 + c * 32, v);
-#pragma unroll
-        for (int k = 0; k < 32; k += 2) {
-          const float d0 = P[c * 32 + k] * (__uint_as_float(v[k]) - dlt);
-          const float d1 = P[c * 32 + k + 1] * (__uint_as_float(v[k + 1]) - dlt);
-          ds[c * 16 + k / 2] = pack_bf16x2(d0, d1);
+        for (int k = 0; k < 64; k += 2) {
+          const float d0 = P[k] * (__uint_as_float(v[k]) - dlt);
+          const float d1 = P[k + 1] * (__uint_as_float(v[k + 1]) - dlt);
+          ds[k / 2] = pack_bf16x2(d0, d1);
         }
       }
       tc_fence_before();
@@ -334,10 +352,10 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c, ++chunk) {
         uint32_t v[32];
-        tmem_ld32(tmem + lane_off + L::kColDP + c * 32, v);
+        tmem_ld32(tmem + lane_off + dp_region(it) + c * 32, v);
         if (c == D / 32 - 1) {
           tc_fence_before();
-          mbar_arrive(&B.dp_free);
+          mbar_arrive(&B.dq_free);
         }
         const uint32_t b = chunk & 1;
         if (lane == 0) bulk_wait_group_read<1>();            // the reduce that last read stage b is done

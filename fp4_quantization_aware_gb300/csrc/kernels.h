@@ -40,6 +40,8 @@ cudaError_t launch_bwd(const Problem& p, const bf16* qh, const bf16* kh, const b
                        const float* lse, const float* delta, float* dq_acc, bf16* dk, bf16* dv, uint32_t* err,
                        cudaStream_t st);
 
+cudaError_t launch_quotient_selftest(unsigned long long* out, cudaStream_t st);
+
 cudaError_t launch_wait_timeout(uint32_t* err, uint64_t timeout_ns, cudaStream_t st);
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link

@@ -153,6 +153,39 @@ __global__ void wait_timeout_kernel(uint32_t* err, uint64_t timeout_ns) {
   __syncthreads();
 }
 
+// Every E4M3 scale s (126 positive values) times every FP32 a of either sign
+// with |a| / s in [1/8, 16): div_by_scale against IEEE division, bit for bit.
+// out[0] counts mismatches; out[1], out[2] keep the bits of one (a, s).
+constexpr int64_t kQuotPerScale = int64_t(7) << 23;   // 7 binades of FP32
+constexpr int64_t kQuotTotal = 126 * kQuotPerScale * 2;
+
+__device__ __forceinline__ float e4m3_value(int code) {   // code 1..126
+  const int e = code >> 3, m = code & 7;
+  return e == 0 ? m * 0x1p-9f : ldexpf(1.0f + m / 8.0f, e - 7);
+}
+
+__global__ void __launch_bounds__(kThreads) quotient_selftest_kernel(unsigned long long* out) {
+  unsigned long long bad = 0;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < kQuotTotal;
+       i += static_cast<int64_t>(gridDim.x) * kThreads) {
+    const int64_t j = i >> 1;
+    const int code = 1 + static_cast<int>(j / kQuotPerScale);
+    const float s = e4m3_value(code);
+    const uint32_t lo = __float_as_uint(s * 0.125f);
+    float a = __uint_as_float(lo + static_cast<uint32_t>(j % kQuotPerScale));
+    if (i & 1) a = -a;
+    const float r = __frcp_rn(s);
+    const float got = copysignf(div_by_scale(a, s, r), a);
+    const float want = __fdiv_rn(a, s);
+    if (__float_as_uint(got) != __float_as_uint(want)) {
+      ++bad;
+      if (atomicCAS(out + 1, 0ull, static_cast<unsigned long long>(__float_as_uint(a)) | 1ull << 32) == 0ull)
+        out[2] = __float_as_uint(s);
+    }
+  }
+  if (bad) atomicAdd(out, bad);
+}
+
 inline unsigned blocks_for(int64_t n) { return static_cast<unsigned>((n + kThreads - 1) / kThreads); }
 
 }  // namespace
@@ -193,6 +226,13 @@ cudaError_t launch_dq_convert(const Problem& p, const float* dq_acc, bf16* dq, c
   const int64_t n4 = p.bh() * p.Sq * p.D / 4;
   dq_convert_kernel<<<blocks_for(n4), kThreads, 0, st>>>(reinterpret_cast<const float4*>(dq_acc),
                                                          reinterpret_cast<uint2*>(dq), n4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quotient_selftest(unsigned long long* out, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(out, 0, 3 * sizeof(unsigned long long), st);
+  if (e != cudaSuccess) return e;
+  quotient_selftest_kernel<<<152 * 8, kThreads, 0, st>>>(out);
   return cudaGetLastError();
 }
 

@@ -158,6 +158,15 @@ attnqat_status attnqat_bwd_noalloc(const attnqat_problem* p, const void* dout, c
  * ATTNQAT_ERR_CUDA if the synchronization failed. clear != 0 resets it. */
 attnqat_status attnqat_device_status(int clear);
 
+/* Checks the quantizer's division-free quotient against IEEE FP32 division,
+ * bit for bit, for every positive E4M3 scale s and every FP32 a of either
+ * sign with |a| / s in [1/8, 16) (about 7.4e9 pairs; below 1/8 the E2M1 code
+ * is 0 and above 16 it saturates either way). `out` is a device pointer to 3
+ * unsigned 64-bit words, written on `stream`: the mismatch count, then the
+ * bits of one mismatching a (| 1 << 32) and s. Supports the "precise
+ * division" requirement of the cuDNN page (Overview). */
+attnqat_status attnqat_selftest_quotient(unsigned long long* out, void* stream);
+
 /* Launches one CTA that waits on a barrier that nothing arrives at, with a
  * limit of timeout_ns nanoseconds; it then records ATTNQAT_ERR_TIMEOUT in the
  * device error word and returns. Exercises the bounded-wait path without

@@ -6,4 +6,5 @@ the CUDA path in ``fp4_quantization_aware_gb300``, and neither imports the
 other.
 """
 from .nvfp4 import fake_nvfp4, fl32, group_scale, quantize_with_scale, rne_e2m1, rne_e4m3  # noqa: F401
-from .attn import attn_qat_bwd, attn_qat_fwd, bwd_head, delta, fwd_head, hats, p_hat, probs  # noqa: F401
+from .attn import (attn_qat_bwd, attn_qat_fwd, bwd_head, delta, dkdv_keys, dq_rows, fwd_head, fwd_rows,  # noqa: F401
+                   hats, lse_ohp_head, p_hat, probs)

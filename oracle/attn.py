@@ -147,6 +147,57 @@ def attn_qat_bwd(do, q, k, v, o_hp, lse, scale, causal=False, quantize=True):
     return dq, dk, dv
 
 
+def lse_ohp_head(qh, kh, vh, scale, causal, block=ROW_BLOCK):
+    """LSE and O' = P V^ of every row of one head (no quantization work)."""
+    Sq = qh.shape[0]
+    o_hp = np.empty((Sq, vh.shape[1]))
+    lse = np.empty(Sq)
+    for r0 in range(0, Sq, block):
+        s = _logits(qh[r0:r0 + block], kh, scale, causal, r0)
+        m = np.max(s, axis=1, keepdims=True)
+        l = m + np.log(np.sum(np.exp(s - m), axis=1, keepdims=True))
+        o_hp[r0:r0 + block] = np.exp(s - l) @ vh
+        lse[r0:r0 + block] = l[:, 0]
+    return o_hp, lse
+
+
+def fwd_rows(qh, kh, vh, scale, causal, r0, r1, quantize=True):
+    """(O, O', LSE) of query rows [r0, r1) of one head (same equations as fwd_head)."""
+    s = _logits(qh[r0:r1], kh, scale, causal, r0)
+    m = np.max(s, axis=1, keepdims=True)
+    l = m + np.log(np.sum(np.exp(s - m), axis=1, keepdims=True))
+    p = np.exp(s - l)
+    return p_hat(p, quantize) @ vh, p @ vh, l[:, 0]
+
+
+def dq_rows(do, qh, kh, vh, o_hp, lse, scale, causal, r0, r1):
+    """dQ of query rows [r0, r1) of one head: scale * dS K^ over all keys."""
+    d = np.sum(o_hp[r0:r1] * do[r0:r1], axis=1)
+    p = np.exp(_logits(qh[r0:r1], kh, scale, causal, r0) - lse[r0:r1, None])
+    ds = p * (do[r0:r1] @ vh.T - d[:, None])
+    return scale * (ds @ kh)
+
+
+def dkdv_keys(do, qh, kh, vh, o_hp, lse, scale, causal, k0, k1, quantize=True):
+    """dK, dV of key rows [k0, k1) of one head, over all query rows.
+
+    k0 must be a multiple of 16 and k1 a multiple of 16 or the key count, so
+    that the block holds whole probability groups (groups start at key 0)."""
+    if k0 % 16 or (k1 % 16 and k1 != kh.shape[0]):
+        raise ValueError("key block must hold whole 16-key groups")
+    d = np.sum(o_hp * do, axis=1)
+    s = scale * (qh @ kh[k0:k1].T)
+    if causal:
+        i = np.arange(qh.shape[0])[:, None]
+        j = np.arange(k0, k1)[None, :]
+        s = np.where(j > i, -np.inf, s)
+    p = np.exp(s - lse[:, None])
+    dv = p_hat(p, quantize).T @ do
+    ds = p * (do @ vh[k0:k1].T - d[:, None])
+    dk = scale * (ds.T @ qh)
+    return dk, dv
+
+
 def delta(o_hp, do):
     """The backward's preprocessing statistic rowsum(O' * dO), float64."""
     return np.sum(np.asarray(o_hp, np.float64) * np.asarray(do, np.float64), axis=-1)

@@ -170,3 +170,30 @@ def test_rejects_causal_cross_attention():
     q, k, v, _ = _inputs(1, 1, 8, 12, 16, 17)
     with pytest.raises(ValueError):
         attn.attn_qat_fwd(q, k, v, 0.25, causal=True)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_sampled_row_and_key_blocks_agree_with_whole_head(causal):
+    """The sampled-block helpers used at full size equal slices of the whole-head oracle."""
+    q, k, v, do = _inputs(1, 1, 70, 70, 16, 18, gain=3.0)
+    scale = 0.4
+    qh, kh, vh = (nvfp4.fake_nvfp4(t[0, 0]) for t in (q, k, v))
+    do = do[0, 0]
+    o, o_hp, lse = attn.fwd_head(qh, kh, vh, scale, causal)
+    dq, dk, dv = attn.bwd_head(do, qh, kh, vh, o_hp, lse, scale, causal)
+    o2, ohp2 = attn.lse_ohp_head(qh, kh, vh, scale, causal)
+    np.testing.assert_allclose(o2, o_hp, rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(ohp2, lse, rtol=1e-13)
+    for r0, r1 in ((0, 5), (30, 47), (60, 70)):
+        fo, fohp, flse = attn.fwd_rows(qh, kh, vh, scale, causal, r0, r1)
+        np.testing.assert_allclose(fo, o[r0:r1], rtol=1e-12, atol=1e-15)
+        np.testing.assert_allclose(fohp, o_hp[r0:r1], rtol=1e-12, atol=1e-15)
+        np.testing.assert_allclose(flse, lse[r0:r1], rtol=1e-13)
+        np.testing.assert_allclose(attn.dq_rows(do, qh, kh, vh, o_hp, lse, scale, causal, r0, r1), dq[r0:r1],
+                                   rtol=1e-10, atol=1e-13)
+    for k0, k1 in ((0, 16), (32, 64), (64, 70)):
+        bk, bv = attn.dkdv_keys(do, qh, kh, vh, o_hp, lse, scale, causal, k0, k1)
+        np.testing.assert_allclose(bk, dk[k0:k1], rtol=1e-10, atol=1e-13)
+        np.testing.assert_allclose(bv, dv[k0:k1], rtol=1e-10, atol=1e-13)
+    with pytest.raises(ValueError):
+        attn.dkdv_keys(do, qh, kh, vh, o_hp, lse, scale, causal, 8, 24)

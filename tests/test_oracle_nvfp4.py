@@ -194,3 +194,17 @@ def test_worked_groups():
         np.testing.assert_array_equal(got.view(np.int64), want.view(np.int64), err_msg=name)
         n += 1
     assert n == 5
+
+
+def test_device_zero_scale_threshold_is_exact():
+    """The kernels skip the quantizer for groups with amax <= kZeroScaleAmax;
+    that constant must be exactly the largest FP32 amax whose scale is zero."""
+    import re
+    src = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                            "fp4_quantization_aware_gb300", "csrc", "nvfp4.cuh")).read()
+    t = np.float32(float(re.search(r"kZeroScaleAmax = ([0-9.e+-]+)f", src).group(1)))
+    up = np.nextafter(t, np.float32(1))
+    assert nvfp4.group_scale(np.float64(t)) == 0.0
+    assert nvfp4.group_scale(np.float64(up)) > 0.0
+    assert nearest_even(np.float64(t / np.float32(6)), E4)[()] == 0.0
+    assert nearest_even(np.float64(up / np.float32(6)), E4)[()] > 0.0

@@ -115,3 +115,16 @@ def test_in_place(lib):
     lib.attnqat_fake_nvfp4(t.data_ptr(), t.data_ptr(), 64, 128, torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     assert torch.equal(t, ref)
+
+
+def test_quotient_matches_ieee_division_exhaustively(lib):
+    """The quantizer divides by the group scale without a division instruction;
+    on every E4M3 scale and every FP32 numerator whose quotient can reach an
+    E2M1 decision, the result equals IEEE division bit for bit."""
+    import torch
+    out = torch.zeros(3, dtype=torch.int64, device="cuda")
+    attnqat.check(lib.attnqat_selftest_quotient(out.data_ptr(), torch.cuda.current_stream().cuda_stream),
+                  "selftest_quotient")
+    torch.cuda.synchronize()
+    n, a_bits, s_bits = out.cpu().tolist()
+    assert n == 0, f"{n} mismatches, e.g. a bits {a_bits & 0xFFFFFFFF:#x}, s bits {s_bits:#x}"
