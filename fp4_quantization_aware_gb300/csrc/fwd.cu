@@ -215,13 +215,11 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       if (!warp_wait(&B.s_full[s], (t >> 1) & 1, ctl)) { ok = false; break; }
       tc_fence_after();
       float x[64];
+      {
+        uint32_t v[64];
+        tmem_ld64(tmem + lane_off + L::kColS0 + s * 128 + half * 64, v);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_off + L::kColS0 + s * 128 + half * 64 + c * 32, v);
-#pragma unroll
-        for (int k = 0; k < 32; ++k)
-          x[c * 32 + k] = (c * 32 + k < valid) ? __uint_as_float(v[k]) * a.c2 : -INFINITY;
+        for (int k = 0; k < 64; ++k) x[k] = (k < valid) ? __uint_as_float(v[k]) * a.c2 : -INFINITY;
       }
       tc_fence_before();
       mbar_arrive(&B.s_free[s]);
@@ -270,14 +268,13 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       if (!warp_wait(&B.s_full[s], (t >> 1) & 1, ctl)) { ok = false; break; }
       tc_fence_after();
       float P[64];
+      {
+        uint32_t v[64];
+        tmem_ld64(tmem + lane_off + L::kColS0 + s * 128 + half * 64, v);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_off + L::kColS0 + s * 128 + half * 64 + c * 32, v);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
+        for (int k = 0; k < 64; ++k) {
           const float p = ex2(fmaf(__uint_as_float(v[k]), a.c2, -lse2));
-          P[c * 32 + k] = (c * 32 + k < valid) ? p : 0.0f;
+          P[k] = (k < valid) ? p : 0.0f;
         }
       }
       tc_fence_before();
