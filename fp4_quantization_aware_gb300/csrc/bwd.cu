@@ -40,7 +40,6 @@ namespace {
 constexpr int kThreadsBwd = 14 * 32;
 constexpr int kWarpTma = 12;
 constexpr int kWarpMma = 13;
-constexpr int kWarpDq0 = 8;
 
 template <int D>
 struct BwdLayout {
@@ -56,8 +55,6 @@ struct BwdLayout {
   static constexpr uint32_t kBytes = kBar + 256;
   static constexpr uint32_t kAlloc = kBytes + 1024;      // room to align the base to 1024
   // TMEM columns
-  static constexpr uint32_t kColR0 = 0;      // S / dP / dQ region 0
-  static constexpr uint32_t kColR1 = 128;    // S / dP / dQ region 1
   static constexpr uint32_t kColDV = 256;
   static constexpr uint32_t kColDK = 256 + D;
 };
@@ -82,6 +79,8 @@ struct BwdBars {
   uint64_t buf_free;
   uint64_t dq_full;
   uint64_t drain;
+  uint64_t peer_free;   // rank 1: rank 0's shared memory may receive the partial dK/dV
+  uint64_t peer_data;   // rank 0: rank 1's partial dK/dV rows have landed
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
@@ -92,8 +91,9 @@ struct BwdArgs {
   bf16* dk;
   bf16* dv;
   int Sq, Sk;
-  int n_qtiles;
+  int n_qtiles, n_ktiles;
   int causal;
+  int split;  // 1: a cluster of 2 CTAs shares each key tile, each taking half its query tiles
   float scale;
   float c2;   // scale * log2(e)
   uint32_t* err;
@@ -113,10 +113,20 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
 
   const int warp = warp_id();
   const int lane = lane_id();
-  const int j = blockIdx.x;                 // key tile
-  const int bh = blockIdx.y;
-  const int i_begin = a.causal ? j : 0;     // BM == BN: the diagonal tile index equals j
-  const int n_it = a.n_qtiles - i_begin;
+  // 1-D grid, key tiles fastest. With a split, CTAs 2p and 2p+1 form a cluster
+  // on key tile p: rank 0 takes the first half of its query tiles (rounded up),
+  // rank 1 the rest, and rank 0 stores the summed dK, dV.
+  const int lin = static_cast<int>(blockIdx.x);
+  const int rank = a.split ? (lin & 1) : 0;
+  const int pair = a.split ? (lin >> 1) : lin;
+  const int j = pair % a.n_ktiles;          // key tile
+  const int bh = pair / a.n_ktiles;
+  const int i_first = a.causal ? j : 0;     // BM == BN: the diagonal tile index equals j
+  const int n_total = a.n_qtiles - i_first;
+  const int n_half0 = a.split ? (n_total + 1) / 2 : n_total;
+  const int i_begin = rank == 0 ? i_first : i_first + n_half0;
+  const int n_it = rank == 0 ? n_half0 : n_total - n_half0;
+  const int peer_n_it = a.split ? (rank == 0 ? n_total - n_half0 : n_half0) : 0;
 
   if (threadIdx.x == 0) {
     B.abort_flag = 0;
@@ -134,6 +144,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     mbar_init(&B.buf_free, 1);
     mbar_init(&B.dq_full, 1);
     mbar_init(&B.drain, 1);
+    mbar_init(&B.peer_free, 1);
+    mbar_init(&B.peer_data, 256);
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -142,13 +154,14 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (a.split) cluster_sync();   // the peer's barriers are initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem = B.tmem_base;
   const WaitCtl ctl{&B.abort_flag, a.err, a.timeout_ns};
 
   if (warp == kWarpTma) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    if (lane == 0 && n_it > 0) {
       tma_prefetch_desc(&tm_q), tma_prefetch_desc(&tm_k), tma_prefetch_desc(&tm_v), tma_prefetch_desc(&tm_do);
       int q_uses[2] = {0, 0}, do_uses = 0;
       mbar_arrive_expect_tx(&B.kv_full, 2 * L::kTile);
@@ -211,7 +224,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         }
       };
 
-      bool ok = mbar_wait(&B.kv_full, 0, ctl) && mbar_wait(&B.q_full[0], 0, ctl);
+      bool ok = n_it > 0 && mbar_wait(&B.kv_full, 0, ctl) && mbar_wait(&B.q_full[0], 0, ctl);
       if (ok) {
         tc_fence_after();
         mma_nt(L::kQ0, L::kK, s_region(0));
@@ -323,24 +336,56 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       fence_proxy_async_smem();
       mbar_arrive(&B.ds_ready);
     }
-    // Epilogue: warps 0-3 write dK (scaled), warps 4-7 write dV, one key row each.
-    if (ok && warp_wait(&B.buf_free, (n_it - 1) & 1, ctl)) {
+    // Epilogue: warps 0-3 own dK rows (scaled), warps 4-7 dV rows, one key row
+    // per thread. With a split key tile, rank 1 writes its FP32 partial rows
+    // into rank 0's shared memory ([dK | dV][128 rows][D floats], 16-byte
+    // chunks swizzled by row) once rank 0's operands are no longer needed, and
+    // rank 0 stores the sums.
+    const int krow = j * 128 + r;
+    const uint32_t col = half == 0 ? L::kColDK : L::kColDV;
+    const float mul = half == 0 ? a.scale : 1.0f;
+    const uint32_t prow = half * (128u * D * 4u) + r * (D * 4u);
+    if (ok && n_it > 0 && warp_wait(&B.buf_free, (n_it - 1) & 1, ctl)) {
       tc_fence_after();
-      const int krow = j * 128 + r;
-      const uint32_t col = half == 0 ? L::kColDK : L::kColDV;
-      const float mul = half == 0 ? a.scale : 1.0f;
-      bf16* out = (half == 0 ? a.dk : a.dv) + ((size_t)bh * a.Sk + krow) * D;
+      if (rank == 1) {
+        if (warp_wait_cluster(&B.peer_free, 0, ctl)) {
+          const uint32_t dst = mapa_shared(sbase + prow, 0);
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_off + col + c * 32, v);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_off + col + c * 32, v);
-        if (krow < a.Sk) store_row32_bf16(out + c * 32, v, mul);
+            for (int q = 0; q < 8; ++q)
+              st_cluster_v4(dst + (((c * 8 + q) ^ (r & 7)) << 4), v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          }
+          mbar_arrive_remote(mapa_shared(smem_u32(&B.peer_data), 0));
+        }
+      } else {
+        // This CTA's MMAs are done: its operand tiles may be overwritten.
+        if (peer_n_it > 0 && warp == 0 && lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&B.peer_free), 1));
+        const bool add_peer = peer_n_it > 0 && warp_wait_cluster(&B.peer_data, 0, ctl);
+        bf16* out = (half == 0 ? a.dk : a.dv) + ((size_t)bh * a.Sk + krow) * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_off + col + c * 32, v);
+          if (add_peer) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float4 pv = *reinterpret_cast<const float4*>(smem + prow + (((c * 8 + q) ^ (r & 7)) << 4));
+              v[4 * q] = __float_as_uint(__uint_as_float(v[4 * q]) + pv.x);
+              v[4 * q + 1] = __float_as_uint(__uint_as_float(v[4 * q + 1]) + pv.y);
+              v[4 * q + 2] = __float_as_uint(__uint_as_float(v[4 * q + 2]) + pv.z);
+              v[4 * q + 3] = __float_as_uint(__uint_as_float(v[4 * q + 3]) + pv.w);
+            }
+          }
+          if (krow < a.Sk) store_row32_bf16(out + c * 32, v, mul);
+        }
       }
     }
   } else {
     // ------------------------------------------------------------ dQ drain (warps 8-11)
     const uint32_t quarter = warp & 3;
-    const uint32_t r = quarter * 32 + lane;
     const uint32_t lane_off = (quarter * 32u) << 16;
     const uint32_t stage0 = sbase + L::kDQ + quarter * 8192;   // two 4 KiB stages of 32 rows x 128 B
     uint8_t* stage0_ptr = smem + L::kDQ + quarter * 8192;
@@ -380,6 +425,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (a.split) cluster_sync();   // no CTA leaves while its peer may still reach its shared memory
   if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -401,18 +447,46 @@ cudaError_t launch_bwd(const Problem& p, const bf16* qh, const bf16* kh, const b
   a.lse = lse, a.delta = delta, a.dk = dk, a.dv = dv;
   a.Sq = static_cast<int>(p.Sq), a.Sk = static_cast<int>(p.Sk);
   a.n_qtiles = static_cast<int>((p.Sq + kBlockM - 1) / kBlockM);
+  a.n_ktiles = static_cast<int>((p.Sk + kBlockN - 1) / kBlockN);
   a.causal = p.causal ? 1 : 0;
   a.scale = p.scale, a.c2 = p.scale * kLog2e;
   a.err = err, a.timeout_ns = kWaitTimeoutNs;
-  const dim3 grid(static_cast<unsigned>((p.Sk + kBlockN - 1) / kBlockN), static_cast<unsigned>(bh));
+  // Split each key tile's query tiles between a cluster of 2 CTAs when even
+  // the split grid fits in one wave: then it halves the time of the only wave.
+  // With more key tiles the split's per-CTA costs (operand loads, pipeline
+  // fill and drain, the partial dK/dV exchange) outweigh the gain (measured on
+  // B=1 H=16 S=4096: 715 vs 779 TFLOP/s).
+  int sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    sms = 148;
+  const int64_t tiles = static_cast<int64_t>(a.n_ktiles) * static_cast<int64_t>(bh);
+  a.split = (2 * tiles <= static_cast<int64_t>(sms) && a.n_qtiles > 1) ? 1 : 0;
+  const int64_t blocks = tiles * (a.split ? 2 : 1);
+  if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+  cfg.blockDim = dim3(kThreadsBwd, 1, 1);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = a.split ? 2 : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (p.D == 128) {
     cudaError_t e = set_smem(reinterpret_cast<const void*>(&bwd_kernel<128>), BwdLayout<128>::kAlloc);
     if (e != cudaSuccess) return e;
-    bwd_kernel<128><<<grid, kThreadsBwd, BwdLayout<128>::kAlloc, st>>>(tq, tk, tv, tdo, tdq, a);
+    cfg.dynamicSmemBytes = BwdLayout<128>::kAlloc;
+    e = cudaLaunchKernelEx(&cfg, bwd_kernel<128>, tq, tk, tv, tdo, tdq, a);
+    if (e != cudaSuccess) return e;
   } else {
     cudaError_t e = set_smem(reinterpret_cast<const void*>(&bwd_kernel<64>), BwdLayout<64>::kAlloc);
     if (e != cudaSuccess) return e;
-    bwd_kernel<64><<<grid, kThreadsBwd, BwdLayout<64>::kAlloc, st>>>(tq, tk, tv, tdo, tdq, a);
+    cfg.dynamicSmemBytes = BwdLayout<64>::kAlloc;
+    e = cudaLaunchKernelEx(&cfg, bwd_kernel<64>, tq, tk, tv, tdo, tdq, a);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }
