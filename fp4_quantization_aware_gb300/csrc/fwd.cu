@@ -15,9 +15,14 @@
 // rescaling.
 //
 // TMEM columns: S double-buffered [0,128) and [128,256); O' [256,256+D);
-// O [256+D,256+2D). Warp roles (10 warps): 0-7 softmax (warp w: lanes
-// 32*(w%4).., key columns [64*(w/4), +64)); 8 TMA producer; 9 MMA issuer.
-// Shared memory (D = 128): Q^ 32K, K^ x2 64K, V^ x2 64K, P 32K, P^ 32K.
+// O [256+D,256+2D). In pass 2 the softmax warps write P and P^ (BF16 pairs)
+// back over the S tile they read: the warps of key half h (keys 64h..64h+63)
+// put P in columns 64h + [0,32) and P^ in 64h + [32,64) of that S buffer,
+// columns only they read, and the O' and O MMAs take their A operand from
+// TMEM there. The next S goes into a buffer once the MMAs reading its P are
+// done. Warp roles (10 warps): 0-7 softmax (warp w: lanes 32*(w%4).., key
+// columns [64*(w/4), +64)); 8 TMA producer; 9 MMA issuer.
+// Shared memory (D = 128): Q^ 32K, K^ x2 64K, V^ x2 64K.
 #include "attn_common.cuh"
 
 namespace attnqat {
@@ -35,9 +40,7 @@ struct FwdLayout {
   static constexpr uint32_t kK1 = kK0 + kTile;
   static constexpr uint32_t kV0 = kK1 + kTile;
   static constexpr uint32_t kV1 = kV0 + kTile;
-  static constexpr uint32_t kP = kV1 + kTile;            // 128 x 128 BF16
-  static constexpr uint32_t kPH = kP + 2 * kBlockBytes;  // 128 x 128 BF16
-  static constexpr uint32_t kML = kPH + 2 * kBlockBytes; // 128 rows x (m, l) of half 1, then 128 lse2
+  static constexpr uint32_t kML = kV1 + kTile;           // 128 rows x (m, l) of half 1, then 128 lse2
   static constexpr uint32_t kBar = kML + 1536;
   static constexpr uint32_t kBytes = kBar + 256;
   static constexpr uint32_t kAlloc = kBytes + 1024;
@@ -54,8 +57,9 @@ struct FwdBars {
   uint64_t v_empty[2];
   uint64_t s_full[2];
   uint64_t s_free[2];
-  uint64_t p_ready;
+  uint64_t p_ready[2];   // per S buffer: P and P^ of a pass-2 tile are in TMEM
   uint64_t pv_done;
+  uint64_t o_done;       // one phase: every O' and O MMA has completed
   uint64_t ml_ready;
   uint64_t lse_ready;
   uint64_t drain;
@@ -102,8 +106,10 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       mbar_init(&B.v_full[s], 1), mbar_init(&B.v_empty[s], 1);
       mbar_init(&B.s_full[s], 1), mbar_init(&B.s_free[s], 256);
     }
-    mbar_init(&B.p_ready, 256);
+    mbar_init(&B.p_ready[0], 256);
+    mbar_init(&B.p_ready[1], 256);
     mbar_init(&B.pv_done, 1);
+    mbar_init(&B.o_done, 1);
     mbar_init(&B.ml_ready, 128);
     mbar_init(&B.lse_ready, 128);
     mbar_init(&B.drain, 1);
@@ -158,7 +164,11 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       auto issue_s = [&](int t) -> bool {
         const int s = t & 1;
         if (!mbar_wait(&B.k_full[s], (t >> 1) & 1, ctl)) return false;
-        if (t >= 2 && !mbar_wait(&B.s_free[s], ((t >> 1) - 1) & 1, ctl)) return false;
+        // The buffer's previous tile u = t - 2 must be done with: read by the
+        // softmax warps (pass 1) or its P read by the O' and O MMAs (pass 2).
+        const int u = t - 2;
+        if (u >= 0 && u < nk && !mbar_wait(&B.s_free[s], (u >> 1) & 1, ctl)) return false;
+        if (u >= nk && !mbar_wait(&B.pv_done, (u - nk) & 1, ctl)) return false;
         tc_fence_after();
         const uint32_t kb = s ? L::kK1 : L::kK0;
 #pragma unroll
@@ -171,13 +181,15 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         umma_commit(&B.k_empty[s]);
         return true;
       };
-      // O (+)= A[128 q x 128 keys] V^[128 keys x D]: A K-major, V^ MN-major.
-      auto mma_pv = [&](uint32_t a_off, uint32_t v_off, uint32_t col, bool acc) {
+      // O (+)= A[128 q x 128 keys] V^[128 keys x D]: A from TMEM at `a_col`
+      // (keys 0..63 in columns a_col + [0,32), keys 64..127 in a_col + 64 + [0,32)),
+      // V^ MN-major in shared memory.
+      auto mma_pv = [&](uint32_t a_col, uint32_t v_off, uint32_t col, bool acc) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t oa = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
-          umma_bf16(tmem + col, sdesc_sw128(sbase + a_off + oa, 16, 1024),
-                    sdesc_sw128(sbase + v_off + kk * 2048, kBlockBytes, 1024), kIdO, (acc || kk > 0) ? 1u : 0u);
+          const uint32_t ac = a_col + (kk >> 2) * 64 + (kk & 3) * 8;
+          umma_bf16_tmem_a(tmem + col, tmem + ac, sdesc_sw128(sbase + v_off + kk * 2048, kBlockBytes, 1024), kIdO,
+                           (acc || kk > 0) ? 1u : 0u);
         }
       };
       bool ok = mbar_wait(&B.q_full, 0, ctl) && issue_s(0);
@@ -186,13 +198,18 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         if (t >= nk) {
           const int tv = t - nk, sv = tv & 1;
           if (!mbar_wait(&B.v_full[sv], (tv >> 1) & 1, ctl)) break;
-          if (!mbar_wait(&B.p_ready, tv & 1, ctl)) break;
+          // use index of this tile's S buffer among pass-2 tiles (one barrier
+          // per buffer, so the softmax warps running ahead cannot alias phases)
+          const int pr_use = (t >> 1) - ((nk + 1 - (t & 1)) >> 1);
+          if (!mbar_wait(&B.p_ready[t & 1], pr_use & 1, ctl)) break;
           tc_fence_after();
           const uint32_t vb = sv ? L::kV1 : L::kV0;
-          mma_pv(L::kP, vb, L::kColOP, tv > 0);
-          mma_pv(L::kPH, vb, L::kColO, tv > 0);
+          const uint32_t sc = L::kColS0 + (t & 1) * 128;
+          mma_pv(sc, vb, L::kColOP, tv > 0);        // O' += P V^
+          mma_pv(sc + 32, vb, L::kColO, tv > 0);    // O  += P^ V^
           umma_commit(&B.pv_done);
           umma_commit(&B.v_empty[sv]);
+          if (tv == nk - 1) umma_commit(&B.o_done);
         }
       }
       umma_commit(&B.drain);
@@ -260,8 +277,6 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     }
 
     // pass 2: P = exp2(S * c2 - lse2), P^ = fake_nvfp4(P); hand both to the MMA warp
-    const uint32_t p_block = sbase + L::kP + half * kBlockBytes;
-    const uint32_t ph_block = sbase + L::kPH + half * kBlockBytes;
     for (int t = nk; ok && t < nt; ++t) {
       const int s = t & 1, tv = t - nk;
       const int valid = kend - (tv * 128 + static_cast<int>(half) * 64);
@@ -277,21 +292,21 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
           P[k] = (k < valid) ? p : 0.0f;
         }
       }
-      tc_fence_before();
-      mbar_arrive(&B.s_free[s]);
       uint32_t pw[32], phw[32];
 #pragma unroll
       for (int k = 0; k < 32; ++k) pw[k] = pack_bf16x2(P[2 * k], P[2 * k + 1]);
 #pragma unroll
       for (int g = 0; g < 4; ++g) quant_pack16(P + 16 * g, phw + 8 * g);
-      if (tv > 0 && !warp_wait(&B.pv_done, (tv - 1) & 1, ctl)) { ok = false; break; }
-      store_row64(p_block, r, pw);
-      store_row64(ph_block, r, phw);
-      fence_proxy_async_smem();
-      mbar_arrive(&B.p_ready);
+      // over this warp's own (already read) S columns
+      const uint32_t pcol = tmem + lane_off + L::kColS0 + s * 128 + half * 64;
+      tmem_st32(pcol, pw);
+      tmem_st32(pcol + 32, phw);
+      tc_fence_before();
+      mbar_arrive(&B.p_ready[s]);
     }
     // epilogue: O' and O rows, columns [half*D/2, +D/2)
-    if (ok && warp_wait(&B.pv_done, (nk - 1) & 1, ctl)) {
+    // (a one-shot barrier: the softmax warps may be several pv_done phases ahead)
+    if (ok && warp_wait(&B.o_done, 0, ctl)) {
       tc_fence_after();
       const size_t row = (size_t)bh * a.Sq + qrow;
 #pragma unroll
