@@ -42,6 +42,27 @@ KERNEL_SOURCES = [os.path.join(ROOT, "fp4_quantization_aware_gb300", "csrc", f)
                   for f in ("bwd.cu", "attn_common.cuh", "nvfp4.cuh", "ptx.cuh")]
 
 
+METRIC = "QAT attn bwd TFLOP/s on 1 GB300 (fwd in fwd_tflops); % of dense BF16 peak in roofline"
+
+
+def max_over_ranks(values, device=None):
+    """Element-wise max of per-rank timings over all ranks (the slowest rank
+    sets the job's time). Returns the values unchanged without a process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return list(values)
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_tflops(flops_per_rank_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank does the same work (weak scaling), the
+    job takes as long as its slowest rank."""
+    return world * flops_per_rank_step * steps / (max_ms * 1e-3) / 1e12
+
+
 def kernel_hash() -> str:
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
@@ -208,10 +229,7 @@ def run_ours(args, w, rank, world, local_rank):
 
     res = {"fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "main_ms": main_ms, "step_ms": step_ms, "wall": wall,
            "launches": launches, "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h, "clocks": clk.summary()}
-    if world > 1:
-        v = torch.tensor([bwd_ms, fwd_ms, step_ms, e2e_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(v, op=torch.distributed.ReduceOp.MAX)
-        res["bwd_ms"], res["fwd_ms"], res["step_ms"], res["e2e_ms"] = v.tolist()
+    res["bwd_ms"], res["fwd_ms"], res["step_ms"], res["e2e_ms"] = max_over_ranks([bwd_ms, fwd_ms, step_ms, e2e_ms], dev)
     return res
 
 
@@ -279,7 +297,7 @@ def main():
         bwd_s = sum(r["bwd_s"] for r in per)
         val = sum(r["bwd_flops"] for r in per) / bwd_s / 1e12
         sample = f"backward of head (b=0, h=0) of {w.B * w.H} per step (full {w.Sq}x{w.Sk}), float64 NumPy"
-        line = {"impl": "reference", "metric": "QAT attn bwd TFLOP/s (CPU float64 oracle)", "value": val,
+        line = {"impl": "reference", "metric": METRIC, "value": val,
                 "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": 1e3 * (bwd_s + sum(r["fwd_s"] for r in per)) / args.steps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -299,7 +317,7 @@ def main():
         torch.distributed.destroy_process_group()
         return
     flops_b, flops_f = w.bwd_flops(), w.fwd_flops()
-    value = world * flops_b * args.steps / (r["bwd_ms"] * 1e-3) / 1e12
+    value = job_tflops(flops_b, args.steps, world, r["bwd_ms"])
     main_ms = statistics.mean(r["main_ms"])
     achieved = flops_b / (main_ms * 1e-3) / 1e12
     traffic = None
@@ -308,11 +326,11 @@ def main():
         if prof.get("kernel_hash") == kernel_hash() and prof.get("workload") == w.name:
             traffic = prof.get("dram_bytes_per_launch")
     line = {
-        "metric": "QAT attn bwd TFLOP/s on 1 GB300 (fwd in fwd_tflops); % of dense BF16 peak in roofline",
+        "metric": METRIC,
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": r["step_ms"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic", "config": workload_config(w, l2),
-        "fwd_tflops": world * flops_f * args.steps / (r["fwd_ms"] * 1e-3) / 1e12,
+        "fwd_tflops": job_tflops(flops_f, args.steps, world, r["fwd_ms"]),
         "step_tflops": world * (flops_f + flops_b) / (r["step_ms"] * 1e-3) / 1e12,
         "bwd_ms": r["bwd_ms"] / args.steps, "fwd_ms": r["fwd_ms"] / args.steps,
         "roofline": {"bound": "tensor", "kernel": "bwd_kernel<128> (attnqat_bwd_main)", "achieved": achieved,

@@ -177,3 +177,39 @@ def bwd(do, q, k, v, o_hp, lse, causal=False, scale=None, ws=None, out=None, str
 def device_status(clear: bool = True) -> int:
     """The device error word (0 = ok, 6 = a bounded wait timed out); synchronizes."""
     return load().attnqat_device_status(1 if clear else 0)
+
+
+def _autograd_function():
+    import torch
+
+    class AttnQatFunction(torch.autograd.Function):
+        """O = fake_nvfp4(P) V^ in the forward; the QAT backward (dQ, dK from the
+        unquantized P, dV = fake_nvfp4(P)^T dO) from the saved O' and LSE."""
+
+        @staticmethod
+        def forward(ctx, q, k, v, causal, scale):
+            q, k, v = (t.contiguous() for t in (q, k, v))
+            o, o_hp, lse = fwd(q, k, v, causal=causal, scale=scale)
+            ctx.save_for_backward(q, k, v, o_hp, lse)
+            ctx.causal, ctx.scale = causal, scale
+            return o
+
+        @staticmethod
+        def backward(ctx, do):
+            q, k, v, o_hp, lse = ctx.saved_tensors
+            dq, dk, dv = bwd(do.contiguous(), q, k, v, o_hp, lse, causal=ctx.causal, scale=ctx.scale)
+            return dq, dk, dv, None, None
+
+    return AttnQatFunction
+
+
+_FN = None
+
+
+def attention(q, k, v, causal: bool = False, scale: Optional[float] = None):
+    """Attn-QAT attention for training: BHSD BF16 CUDA tensors in, O out, with
+    the QAT backward wired into autograd."""
+    global _FN
+    if _FN is None:
+        _FN = _autograd_function()
+    return _FN.apply(q, k, v, causal, 1.0 / math.sqrt(q.shape[-1]) if scale is None else scale)

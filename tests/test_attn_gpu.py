@@ -102,3 +102,17 @@ def test_bounded_wait_reports_timeout(lib):
     assert attnqat.device_status(clear=True) == 0
     # the context is still usable afterwards
     run_case(1, 1, 128, 128, 64, False, 2.0)
+
+
+def test_autograd_function_matches_the_c_abi(lib):
+    import torch
+    q, k, v, do = (bf16_dev(a) for a in make_inputs(1, 2, 200, 200, 128, 2.0, 21))
+    q.requires_grad_(), k.requires_grad_(), v.requires_grad_()
+    o = attnqat.attention(q, k, v, causal=True)
+    o.backward(do)
+    o2, o_hp, lse = attnqat.fwd(q.detach(), k.detach(), v.detach(), causal=True)
+    dq, dk, dv = attnqat.bwd(do, q.detach(), k.detach(), v.detach(), o_hp, lse, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2)
+    assert torch.equal(k.grad, dk) and torch.equal(v.grad, dv)
+    assert (q.grad.float() - dq.float()).abs().max().item() <= 1e-2 * dq.float().abs().max().item()
