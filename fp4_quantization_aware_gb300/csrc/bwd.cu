@@ -194,34 +194,36 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);   // S, dP
       constexpr uint32_t kIdT = idesc_bf16(128, D, true, true);       // dV, dK
       constexpr uint32_t kIdQ = idesc_bf16(128, D, false, true);      // dQ
+      // Descriptors are built once and advanced by constants per k-step: the
+      // issuing thread shares its SM sub-partition with two softmax warps, so
+      // few instructions per MMA keep the tensor pipe fed.
+      const uint64_t kmaj = sdesc_sw128(sbase, 16, 1024);             // K-major view at offset 0
+      const uint64_t mnmaj = sdesc_sw128(sbase, kBlockBytes, 1024);   // MN-major view at offset 0
       // X[128 x 128] = A[128 x D] B[128 x D]^T, both K-major (K = D).
       auto mma_nt = [&](uint32_t a_off, uint32_t b_off, uint32_t col) {
+        const uint64_t da = sdesc_advance(kmaj, a_off), db = sdesc_advance(kmaj, b_off);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t o = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
-          umma_bf16(tmem + col, sdesc_sw128(sbase + a_off + o, 16, 1024), sdesc_sw128(sbase + b_off + o, 16, 1024),
-                    kIdS, kk > 0);
+          umma_bf16(tmem + col, sdesc_advance(da, o), sdesc_advance(db, o), kIdS, kk > 0);
         }
       };
       // X[128 keys x D] (+)= A^T B with A = [128 q x 128 keys] and B = [128 q x D],
       // both read MN-major (K = 128 query rows, 16 per step).
       auto mma_tn = [&](uint32_t a_off, uint32_t b_off, uint32_t col, bool acc) {
+        const uint64_t da = sdesc_advance(mnmaj, a_off), db = sdesc_advance(mnmaj, b_off);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t o = kk * 2048;
-          umma_bf16(tmem + col, sdesc_sw128(sbase + a_off + o, kBlockBytes, 1024),
-                    sdesc_sw128(sbase + b_off + o, kBlockBytes, 1024), kIdT, (acc || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16(tmem + col, sdesc_advance(da, kk * 2048), sdesc_advance(db, kk * 2048), kIdT,
+                    (acc || kk > 0) ? 1u : 0u);
       };
       // dQ[128 q x D] = dS[128 q x 128 keys] K^[128 keys x D]: A K-major, B MN-major.
       auto mma_dq = [&](uint32_t col) {
+        const uint64_t da = sdesc_advance(kmaj, L::kPS), db = sdesc_advance(mnmaj, L::kK);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t oa = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
-          const uint32_t ob = kk * 2048;
-          umma_bf16(tmem + col, sdesc_sw128(sbase + L::kPS + oa, 16, 1024),
-                    sdesc_sw128(sbase + L::kK + ob, kBlockBytes, 1024), kIdQ, kk > 0);
-        }
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16(tmem + col, sdesc_advance(da, (kk >> 2) * kBlockBytes + (kk & 3) * 32),
+                    sdesc_advance(db, kk * 2048), kIdQ, kk > 0);
       };
 
       bool ok = n_it > 0 && mbar_wait(&B.kv_full, 0, ctl) && mbar_wait(&B.q_full[0], 0, ctl);

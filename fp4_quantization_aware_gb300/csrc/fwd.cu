@@ -58,7 +58,6 @@ struct FwdBars {
   uint64_t s_full[2];
   uint64_t s_free[2];
   uint64_t p_ready[2];   // per S buffer: P and P^ of a pass-2 tile are in TMEM
-  uint64_t pv_done;
   uint64_t o_done;       // one phase: every O' and O MMA has completed
   uint64_t ml_ready;
   uint64_t lse_ready;
@@ -108,7 +107,6 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     }
     mbar_init(&B.p_ready[0], 256);
     mbar_init(&B.p_ready[1], 256);
-    mbar_init(&B.pv_done, 1);
     mbar_init(&B.o_done, 1);
     mbar_init(&B.ml_ready, 128);
     mbar_init(&B.lse_ready, 128);
@@ -161,21 +159,28 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t kIdO = idesc_bf16(128, D, false, true);
+      // Descriptors built once, advanced by constants per k-step (few issue
+      // instructions per MMA for a thread that shares its sub-partition).
+      const uint64_t kmaj = sdesc_sw128(sbase, 16, 1024);
+      const uint64_t mnmaj = sdesc_sw128(sbase, kBlockBytes, 1024);
+      const uint64_t dq = sdesc_advance(kmaj, L::kQ);
       auto issue_s = [&](int t) -> bool {
         const int s = t & 1;
         if (!mbar_wait(&B.k_full[s], (t >> 1) & 1, ctl)) return false;
-        // The buffer's previous tile u = t - 2 must be done with: read by the
-        // softmax warps (pass 1) or its P read by the O' and O MMAs (pass 2).
+        // The buffer's previous tile u = t - 2 must be done with. A pass-1 S is
+        // done once the softmax warps have read it. A pass-2 buffer holds P(u),
+        // which the O' and O MMAs of tile u read; those were issued by this
+        // thread before this S MMA, and tcgen05.mma operations of one thread
+        // execute in issue order, so no wait is needed (the tensor pipe keeps
+        // running instead of draining once per tile).
         const int u = t - 2;
         if (u >= 0 && u < nk && !mbar_wait(&B.s_free[s], (u >> 1) & 1, ctl)) return false;
-        if (u >= nk && !mbar_wait(&B.pv_done, (u - nk) & 1, ctl)) return false;
         tc_fence_after();
-        const uint32_t kb = s ? L::kK1 : L::kK0;
+        const uint64_t db = sdesc_advance(kmaj, s ? L::kK1 : L::kK0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t o = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
-          umma_bf16(tmem + L::kColS0 + s * 128, sdesc_sw128(sbase + L::kQ + o, 16, 1024),
-                    sdesc_sw128(sbase + kb + o, 16, 1024), kIdS, kk > 0);
+          umma_bf16(tmem + L::kColS0 + s * 128, sdesc_advance(dq, o), sdesc_advance(db, o), kIdS, kk > 0);
         }
         umma_commit(&B.s_full[s]);
         umma_commit(&B.k_empty[s]);
@@ -185,11 +190,11 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       // (keys 0..63 in columns a_col + [0,32), keys 64..127 in a_col + 64 + [0,32)),
       // V^ MN-major in shared memory.
       auto mma_pv = [&](uint32_t a_col, uint32_t v_off, uint32_t col, bool acc) {
+        const uint64_t dv = sdesc_advance(mnmaj, v_off);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t ac = a_col + (kk >> 2) * 64 + (kk & 3) * 8;
-          umma_bf16_tmem_a(tmem + col, tmem + ac, sdesc_sw128(sbase + v_off + kk * 2048, kBlockBytes, 1024), kIdO,
-                           (acc || kk > 0) ? 1u : 0u);
+          umma_bf16_tmem_a(tmem + col, tmem + ac, sdesc_advance(dv, kk * 2048), kIdO, (acc || kk > 0) ? 1u : 0u);
         }
       };
       bool ok = mbar_wait(&B.q_full, 0, ctl) && issue_s(0);
@@ -207,7 +212,6 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
           const uint32_t sc = L::kColS0 + (t & 1) * 128;
           mma_pv(sc, vb, L::kColOP, tv > 0);        // O' += P V^
           mma_pv(sc + 32, vb, L::kColO, tv > 0);    // O  += P^ V^
-          umma_commit(&B.pv_done);
           umma_commit(&B.v_empty[sv]);
           if (tv == nk - 1) umma_commit(&B.o_done);
         }
@@ -240,14 +244,20 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       }
       tc_fence_before();
       mbar_arrive(&B.s_free[s]);
-      float mx = m;
+      // four independent chains for the row max and the row sum (ILP)
+      float mc[4] = {m, m, m, m};
 #pragma unroll
-      for (int k = 0; k < 64; ++k) mx = fmaxf(mx, x[k]);
+      for (int k = 0; k < 64; k += 4)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) mc[u] = fmaxf(mc[u], x[k + u]);
+      const float mx = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3]));
       if (mx == -INFINITY) continue;
-      float sum = 0.0f;
+      float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-      for (int k = 0; k < 64; ++k) sum += ex2(x[k] - mx);
-      l = l * ex2(m - mx) + sum;
+      for (int k = 0; k < 64; k += 4)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) sc[u] += ex2(x[k + u] - mx);
+      l = l * ex2(m - mx) + ((sc[0] + sc[1]) + (sc[2] + sc[3]));
       m = mx;
     }
     // Combine the two column halves of each row: half 1 hands (m, l) to half
@@ -305,7 +315,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       mbar_arrive(&B.p_ready[s]);
     }
     // epilogue: O' and O rows, columns [half*D/2, +D/2)
-    // (a one-shot barrier: the softmax warps may be several pv_done phases ahead)
+    // (a one-shot barrier committed after the last O' and O MMAs)
     if (ok && warp_wait(&B.o_done, 0, ctl)) {
       tc_fence_after();
       const size_t row = (size_t)bh * a.Sq + qrow;

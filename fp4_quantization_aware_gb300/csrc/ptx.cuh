@@ -256,6 +256,11 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// The descriptor of the same tile `bytes` further on: the 14-bit start
+// address field holds (address >> 4) and shared-memory addresses stay below
+// 2^18, so adding to the low word never carries out of the field.
+__device__ __forceinline__ uint64_t sdesc_advance(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
+
 // 32 TMEM columns of this warp's 32 lanes into 32 registers, waiting for the
 // load inside the same asm block so no use of the values can be hoisted above
 // the wait. Thread t gets lane (taddr.lane + t), columns taddr.col .. +31.
