@@ -198,6 +198,55 @@ def dkdv_keys(do, qh, kh, vh, o_hp, lse, scale, causal, k0, k1, quantize=True):
     return dk, dv
 
 
+def infer_fwd(q, k, v, scale, causal=False, quantize=True):
+    """Inference forward on BHSD float64 arrays: (O, LSE) with O = softmax(scale
+    Q^ K^T) V.
+
+    Q and K are NVFP4 (fake_nvfp4 along D, the values an NVFP4-packed tensor
+    holds) and V stays BF16, as in the FP4 inference path of the Attn-QAT paper
+    summary (Results: block-scaled NVFP4 on QK, BF16 on PV) and the FastVideo
+    attn_qat_infer page (fa4_pv_mode "bf16"). No probability quantization."""
+    q, k, v = (np.asarray(t, np.float64) for t in (q, k, v))
+    if causal and q.shape[2] != k.shape[2]:
+        raise ValueError("causal attention needs Sq == Sk")
+    f = _quantizer(quantize)
+    qh, kh = f(q, axis=-1), f(k, axis=-1)
+    B, H, Sq, _ = q.shape
+    o = np.empty((B, H, Sq, v.shape[3]))
+    lse = np.empty((B, H, Sq))
+    for b in range(B):
+        for h in range(H):
+            o[b, h], lse[b, h] = lse_ohp_head(qh[b, h], kh[b, h], v[b, h], scale, causal)
+    return o, lse
+
+
+def nvfp4_codes(x, axis=-1):
+    """NVFP4 encoding of x along ``axis``: (E2M1 codes, E4M3 scale codes).
+
+    Codes follow the formats' bit layouts: E2M1 = sign (bit 3) and a 3-bit
+    magnitude index into {0, .5, 1, 1.5, 2, 3, 4, 6}; E4M3FN = 4-bit exponent
+    (bias 7) and 3-bit mantissa. Values are those of fake_nvfp4; a zero group
+    scale gives codes 0 (or 8 for -0)."""
+    from .nvfp4 import GROUP, group_scales, quantize_with_scale
+    x = np.asarray(x, np.float64)
+    xm = np.moveaxis(x, axis, -1)
+    n = xm.shape[-1]
+    if n % GROUP:
+        raise ValueError("the encoded axis must be a multiple of 16")
+    s = group_scales(xm, axis=-1)                                   # (..., n/16)
+    y = quantize_with_scale(xm, np.repeat(s, GROUP, axis=-1))
+    safe = np.where(np.repeat(s, GROUP, axis=-1) == 0, 1.0, np.repeat(s, GROUP, axis=-1))
+    mag = np.abs(y) / safe
+    idx = np.searchsorted(np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6]), mag)
+    codes = (idx | np.where(np.signbit(y), 8, 0)).astype(np.uint8)
+    e = np.where(s > 0, np.floor(np.log2(np.where(s > 0, s, 1.0))), 0)
+    normal = s >= 2.0 ** -6
+    m_norm = np.rint((s / np.exp2(e) - 1) * 8)
+    sc = np.where(normal, ((e + 7).astype(np.int64) << 3) | m_norm.astype(np.int64),
+                  np.rint(s / 2.0 ** -9).astype(np.int64))
+    return np.moveaxis(codes, -1, axis), np.moveaxis(sc.astype(np.uint8), -1, axis)
+
+
 def delta(o_hp, do):
     """The backward's preprocessing statistic rowsum(O' * dO), float64."""
     return np.sum(np.asarray(o_hp, np.float64) * np.asarray(do, np.float64), axis=-1)

@@ -197,3 +197,39 @@ def test_sampled_row_and_key_blocks_agree_with_whole_head(causal):
         np.testing.assert_allclose(bv, dv[k0:k1], rtol=1e-10, atol=1e-13)
     with pytest.raises(ValueError):
         attn.dkdv_keys(do, qh, kh, vh, o_hp, lse, scale, causal, 8, 24)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_infer_fwd_identity_matches_sdpa(causal):
+    q, k, v, _ = _inputs(1, 2, 45, 45, 16, 19)
+    o, lse = attn.infer_fwd(q, k, v, 0.3, causal, quantize=False)
+    ref = torch.nn.functional.scaled_dot_product_attention(torch.tensor(q), torch.tensor(k), torch.tensor(v),
+                                                           is_causal=causal, scale=0.3)
+    np.testing.assert_allclose(o, ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_infer_fwd_is_the_auxiliary_output_with_bf16_v():
+    """softmax(scale Q^K^T) V with V unquantized equals O' of the pinned
+    training forward run on the same Q^, K^ and an unquantized V."""
+    q, k, v, _ = _inputs(2, 2, 40, 40, 32, 20, gain=2.0)
+    o, lse = attn.infer_fwd(q, k, v, 0.25, causal=True)
+    qh, kh, _ = attn.hats(q, k, v)
+    for b in range(2):
+        for h in range(2):
+            _, o_hp, l2 = attn.fwd_head(qh[b, h], kh[b, h], v[b, h], 0.25, True)
+            np.testing.assert_allclose(o[b, h], o_hp, rtol=1e-12, atol=1e-14)
+            np.testing.assert_allclose(lse[b, h], l2, rtol=1e-13)
+
+
+def test_nvfp4_codes_decode_to_fake_quantized_values():
+    from test_oracle_nvfp4 import E2, E4
+    rng = np.random.default_rng(21)
+    x = np.concatenate([rng.standard_normal((64, 32)) * 3, rng.standard_normal((8, 32)) * 1e-4,
+                        rng.standard_normal((8, 32)) * 5000]).astype(np.float32).astype(np.float64)
+    x[0, 5] = -0.0
+    codes, sc = attn.nvfp4_codes(x)
+    assert codes.shape == x.shape and sc.shape == (x.shape[0], x.shape[1] // 16)
+    assert codes.max() <= 15 and sc.max() <= 126
+    mag = E2[codes & 7] * np.repeat(E4[sc], 16, axis=1)
+    dec = np.where(codes & 8, -mag, mag)
+    np.testing.assert_array_equal(dec.view(np.int64), nvfp4.fake_nvfp4(x).view(np.int64))
