@@ -57,6 +57,10 @@ SIGNATURES = {
     "attnqat_device_status": (_S, [ctypes.c_int]),
     "attnqat_selftest_wait_timeout": (_S, [ctypes.c_uint64, _P]),
     "attnqat_selftest_quotient": (_S, [_P, _P]),
+    "attnqat_nvfp4_pack": (_S, [_P, _P, _P, ctypes.c_int64, ctypes.c_int64, _P]),
+    "attnqat_infer_fwd_workspace_bytes": (ctypes.c_size_t, [_PP]),
+    "attnqat_infer_fwd_packed": (_S, [_PP, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "attnqat_infer_fwd": (_S, [_PP, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
 }
 
 _lib = None
@@ -172,6 +176,62 @@ def bwd(do, q, k, v, o_hp, lse, causal=False, scale=None, ws=None, out=None, str
     check(lib.attnqat_bwd(ctypes.byref(p), _ptr(do), _ptr(q), _ptr(k), _ptr(v), _ptr(o_hp), _ptr(lse), _ptr(dq),
                           _ptr(dk), _ptr(dv), _ptr(ws), ws.numel(), _stream(stream)), "attnqat_bwd")
     return dq, dk, dv
+
+
+def nvfp4_pack(x, stream=None):
+    """Real NVFP4 encoding along the last axis (a multiple of 16) of a BF16 CUDA
+    tensor: (packed uint8 (..., n/2), scales uint8 E4M3 (..., n/16))."""
+    import torch
+    _bf16_contig(x)
+    cols = x.shape[-1]
+    rows = x.numel() // cols if cols else 0
+    packed = torch.empty(*x.shape[:-1], cols // 2, dtype=torch.uint8, device=x.device)
+    scales = torch.empty(*x.shape[:-1], cols // 16, dtype=torch.uint8, device=x.device)
+    lib = load()
+    check(lib.attnqat_nvfp4_pack(_ptr(x), _ptr(packed), _ptr(scales), rows, cols, _stream(stream)),
+          "attnqat_nvfp4_pack")
+    return packed, scales
+
+
+def infer_fwd(q, k, v, causal=False, scale=None, ws=None, out=None, with_lse=True, stream=None):
+    """Inference forward with NVFP4 Q, K and BF16 V: returns (O, LSE or None)."""
+    import torch
+    _bf16_contig(q, k, v)
+    p = _problem_of(q, k, causal, scale)
+    lib = load()
+    need = lib.attnqat_infer_fwd_workspace_bytes(ctypes.byref(p))
+    if need == 0:
+        check(lib.attnqat_check_support(ctypes.byref(p)), "attnqat_check_support")
+        raise AttnQatError(2, "attnqat_infer_fwd", "the inference forward needs D == 128")
+    if ws is None:
+        ws = workspace(need, q.device)
+    if out is None:
+        o = torch.empty_like(q)
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device) if with_lse else None
+    else:
+        o, lse = out
+    check(lib.attnqat_infer_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(ws),
+                                ws.numel(), _stream(stream)), "attnqat_infer_fwd")
+    return o, lse
+
+
+def infer_fwd_packed(q_fp4, q_sf, k_fp4, k_sf, v, causal=False, scale=None, out=None, with_lse=True,
+                     stream=None):
+    """Inference forward on pre-packed NVFP4 Q, K (``nvfp4_pack`` output, BHS
+    leading axes) and BF16 V: returns (O, LSE or None)."""
+    import torch
+    B, H, Sq, _ = q_fp4.shape
+    D = v.shape[3]
+    p = problem(B, H, Sq, k_fp4.shape[2], D, causal, scale)
+    if out is None:
+        o = torch.empty(B, H, Sq, D, dtype=torch.bfloat16, device=v.device)
+        lse = torch.empty(B, H, Sq, dtype=torch.float32, device=v.device) if with_lse else None
+    else:
+        o, lse = out
+    check(load().attnqat_infer_fwd_packed(ctypes.byref(p), _ptr(q_fp4), _ptr(q_sf), _ptr(k_fp4), _ptr(k_sf),
+                                          _ptr(v), _ptr(o), _ptr(lse), _stream(stream)),
+          "attnqat_infer_fwd_packed")
+    return o, lse
 
 
 def device_status(clear: bool = True) -> int:

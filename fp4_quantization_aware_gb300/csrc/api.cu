@@ -158,6 +158,21 @@ bool make_tile_map(CUtensorMap* m, const void* base, bool fp32, uint64_t inner, 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_fp4_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t outer, uint32_t box_rows) {
+  using Encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  auto enc = reinterpret_cast<Encode>(tensor_map_encoder());
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {64, rows, outer};
+  const cuuint64_t strides[2] = {64, 64 * rows};
+  const cuuint32_t box[3] = {64, box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t set_smem(const void* kernel, int bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
@@ -301,6 +316,78 @@ attnqat_status attnqat_bwd(const attnqat_problem* p, const void* dout, const voi
   ATTNQAT_TRY(attnqat_bwd_preprocess(p, dout, q, k, v, o_hp, ws, ws_bytes, stream));
   ATTNQAT_TRY(attnqat_bwd_main(p, dout, lse, dk, dv, ws, ws_bytes, stream));
   return attnqat_bwd_dq_convert(p, dq, ws, ws_bytes, stream);
+}
+
+attnqat_status attnqat_nvfp4_pack(const void* x, void* packed, void* scales, int64_t rows, int64_t cols,
+                                  void* stream) {
+  if (rows < 0 || cols < 0) return fail(ATTNQAT_ERR_INVALID_ARG, "negative size");
+  if (cols % 16 != 0) return fail(ATTNQAT_ERR_INVALID_ARG, "cols (%lld) is not a multiple of 16", (long long)cols);
+  if (rows == 0 || cols == 0) return ATTNQAT_OK;
+  ATTNQAT_TRY(check_ptrs({x, packed, scales}));
+  ATTNQAT_CUDA(launch_nvfp4_pack(static_cast<const bf16*>(x), static_cast<uint8_t*>(packed),
+                                 static_cast<uint8_t*>(scales), rows, cols, static_cast<cudaStream_t>(stream)),
+               "nvfp4_pack");
+  return ATTNQAT_OK;
+}
+
+namespace {
+
+attnqat_status check_infer(const attnqat_problem* p) {
+  ATTNQAT_TRY(check_problem(p));
+  if (p->D != 128) return fail(ATTNQAT_ERR_UNSUPPORTED, "the inference forward needs D == 128 (got %lld)", (long long)p->D);
+  return ATTNQAT_OK;
+}
+
+struct InferWs {
+  size_t q_fp4, q_sf, k_fp4, k_sf, total;
+};
+
+InferWs infer_layout(const attnqat_problem& p) {
+  const size_t bh = static_cast<size_t>(p.B) * p.H;
+  InferWs w{};
+  size_t off = 0;
+  w.q_fp4 = off, off += round256(bh * p.Sq * 64);
+  w.q_sf = off, off += round256(bh * p.Sq * 8);
+  w.k_fp4 = off, off += round256(bh * p.Sk * 64);
+  w.k_sf = off, off += round256(bh * p.Sk * 8);
+  w.total = off;
+  return w;
+}
+
+}  // namespace
+
+size_t attnqat_infer_fwd_workspace_bytes(const attnqat_problem* p) {
+  return check_infer(p) == ATTNQAT_OK ? infer_layout(*p).total : 0;
+}
+
+attnqat_status attnqat_infer_fwd_packed(const attnqat_problem* p, const void* q_fp4, const void* q_sf,
+                                        const void* k_fp4, const void* k_sf, const void* v, void* o, float* lse,
+                                        void* stream) {
+  ATTNQAT_TRY(check_infer(p));
+  ATTNQAT_TRY(check_ptrs({q_fp4, q_sf, k_fp4, k_sf, v, o}));
+  if (lse != nullptr && !aligned16(lse)) return fail(ATTNQAT_ERR_MISALIGNED, "lse is not 16-byte aligned");
+  attnqat_status st = ATTNQAT_OK;
+  uint32_t* err = device_error_word(&st);
+  if (!err) return st;
+  ATTNQAT_CUDA(launch_infer(to_problem(*p), static_cast<const uint8_t*>(q_fp4), static_cast<const uint8_t*>(q_sf),
+                            static_cast<const uint8_t*>(k_fp4), static_cast<const uint8_t*>(k_sf),
+                            static_cast<const bf16*>(v), static_cast<bf16*>(o), lse, err,
+                            static_cast<cudaStream_t>(stream)),
+               "infer_fwd");
+  return ATTNQAT_OK;
+}
+
+attnqat_status attnqat_infer_fwd(const attnqat_problem* p, const void* q, const void* k, const void* v, void* o,
+                                 float* lse, void* ws, size_t ws_bytes, void* stream) {
+  ATTNQAT_TRY(check_infer(p));
+  ATTNQAT_TRY(check_ptrs({q, k, v, o}));
+  const InferWs w = infer_layout(*p);
+  ATTNQAT_TRY(check_ws(ws, ws_bytes, w.total));
+  const int64_t bh = p->B * p->H;
+  ATTNQAT_TRY(attnqat_nvfp4_pack(q, at<uint8_t>(ws, w.q_fp4), at<uint8_t>(ws, w.q_sf), bh * p->Sq, p->D, stream));
+  ATTNQAT_TRY(attnqat_nvfp4_pack(k, at<uint8_t>(ws, w.k_fp4), at<uint8_t>(ws, w.k_sf), bh * p->Sk, p->D, stream));
+  return attnqat_infer_fwd_packed(p, at<uint8_t>(ws, w.q_fp4), at<uint8_t>(ws, w.q_sf), at<uint8_t>(ws, w.k_fp4),
+                                  at<uint8_t>(ws, w.k_sf), v, o, lse, stream);
 }
 
 attnqat_status attnqat_device_status(int clear) {

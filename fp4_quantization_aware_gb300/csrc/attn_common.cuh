@@ -93,6 +93,11 @@ __device__ __forceinline__ void store_row32_bf16(bf16* dst, const uint32_t (&v)[
 bool make_tile_map(CUtensorMap* m, const void* base, bool fp32, uint64_t inner, uint64_t rows, uint64_t outer,
                    uint32_t box_inner, uint32_t box_rows);
 
+// 3-D tiled tensor map over packed NVFP4 data, (outer, rows, 64 bytes) with
+// two E2M1 values per byte (D = 128), a {64, box_rows, 1} box and the 64-byte
+// swizzle; rows past `rows` read as zero.
+bool make_fp4_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t outer, uint32_t box_rows);
+
 // Opt the kernel into `bytes` of dynamic shared memory (once per kernel).
 cudaError_t set_smem(const void* kernel, int bytes);
 

@@ -31,6 +31,9 @@ cudaError_t launch_prep(const Problem& p, const bf16* q, const bf16* k, const bf
                         const bf16* dout, bf16* qh, bf16* kh, bf16* vh, float* delta, float* dq_acc,
                         cudaStream_t st);
 
+cudaError_t launch_nvfp4_pack(const bf16* x, uint8_t* packed, uint8_t* scales, int64_t rows, int64_t cols,
+                              cudaStream_t st);
+
 cudaError_t launch_dq_convert(const Problem& p, const float* dq_acc, bf16* dq, cudaStream_t st);
 
 cudaError_t launch_fwd(const Problem& p, const bf16* qh, const bf16* kh, const bf16* vh, bf16* o, bf16* o_hp,
@@ -39,6 +42,12 @@ cudaError_t launch_fwd(const Problem& p, const bf16* qh, const bf16* kh, const b
 cudaError_t launch_bwd(const Problem& p, const bf16* qh, const bf16* kh, const bf16* vh, const bf16* dout,
                        const float* lse, const float* delta, float* dq_acc, bf16* dk, bf16* dv, uint32_t* err,
                        cudaStream_t st);
+
+// Inference forward: O = softmax(scale * Q K^T) V with packed NVFP4 Q and K
+// ((B*H, S, 64) bytes of E2M1 pairs, (B*H, S, 8) E4M3 scales) and BF16 V;
+// lse may be null. D = 128 only.
+cudaError_t launch_infer(const Problem& p, const uint8_t* q_fp4, const uint8_t* q_sf, const uint8_t* k_fp4,
+                         const uint8_t* k_sf, const bf16* v, bf16* o, float* lse, uint32_t* err, cudaStream_t st);
 
 cudaError_t launch_quotient_selftest(unsigned long long* out, cudaStream_t st);
 

@@ -84,6 +84,24 @@ __global__ void __launch_bounds__(kThreads) fake_f32_kernel(const float* x, floa
     if (c0 + i < cols) y[base + i] = f[i];
 }
 
+// ------------------------------------------------------------ NVFP4 packing
+// One thread per 16-value group of a BF16 (rows, cols) matrix, cols % 16 == 0:
+// 8 bytes of E2M1 pairs to `packed` (row-major, cols/2 bytes per row) and one
+// E4M3 scale byte to `scales` (cols/16 per row).
+__global__ void __launch_bounds__(kThreads) nvfp4_pack_kernel(const bf16* __restrict__ x, uint8_t* __restrict__ packed,
+                                                              uint8_t* __restrict__ scales, int64_t groups) {
+  const int64_t g = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+  if (g >= groups) return;
+  float f[16];
+  load16(x + g * 16, f);
+  uint8_t b[8];
+  scales[g] = nvfp4_encode_16(f, b);
+  uint2 w;
+  w.x = b[0] | (uint32_t)b[1] << 8 | (uint32_t)b[2] << 16 | (uint32_t)b[3] << 24;
+  w.y = b[4] | (uint32_t)b[5] << 8 | (uint32_t)b[6] << 16 | (uint32_t)b[7] << 24;
+  reinterpret_cast<uint2*>(packed)[g] = w;
+}
+
 // ------------------------------------------------------------ fused preprocess
 struct PrepArgs {
   const bf16* src[3];   // q, k, v
@@ -219,6 +237,14 @@ cudaError_t launch_prep(const Problem& p, const bf16* q, const bf16* k, const bf
     prep_kernel<128><<<grid, kThreads, 0, st>>>(a);
   else
     prep_kernel<64><<<grid, kThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_nvfp4_pack(const bf16* x, uint8_t* packed, uint8_t* scales, int64_t rows, int64_t cols,
+                              cudaStream_t st) {
+  const int64_t groups = rows * (cols / 16);
+  if (groups == 0) return cudaSuccess;
+  nvfp4_pack_kernel<<<blocks_for(groups), kThreads, 0, st>>>(x, packed, scales, groups);
   return cudaGetLastError();
 }
 

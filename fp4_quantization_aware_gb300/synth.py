@@ -21,6 +21,8 @@ Workloads (BHSD, BF16 activations):
   entries scaled x10 (heavy tail); dO N(0, 0.01), i.e. std 0.1.
 * ``peaked`` B=1 H=2 S=256 D=64 non-causal with logits sharpened (Q x4) so
   that most probability groups survive quantization.
+* ``ctx32k`` B=1 H=16 S=32768 D=128 non-causal, iid N(0,1): the long-context
+  shape the FP4 inference forward is quoted on (dO unused there).
 """
 from __future__ import annotations
 
@@ -69,6 +71,7 @@ WORKLOADS = {
     "c4": Workload("c4", 1, 40, 32760, 32760, 128, False, 1 / math.sqrt(128)),
     "c5": Workload("c5", 1, 64, 16384, 16384, 128, True, 1 / math.sqrt(128), "heavy"),
     "peaked": Workload("peaked", 1, 2, 256, 256, 64, False, 1 / 8, "peaked", 4.0),
+    "ctx32k": Workload("ctx32k", 1, 16, 32768, 32768, 128, False, 1 / math.sqrt(128)),
 }
 
 

@@ -151,6 +151,43 @@ attnqat_status attnqat_bwd_noalloc(const attnqat_problem* p, const void* dout, c
                                    const void* v, const void* o_hp, const float* lse, void* dq, void* dk, void* dv,
                                    void* stream);
 
+/* ---- NVFP4 inference forward ("Attn-QAT: 4-Bit Attention With
+ * Quantization-Aware Training", Results: block-scaled NVFP4 on the QK MMA,
+ * BF16 on PV; FastVideo attn_qat_infer page: Q and K packed to NVFP4 with
+ * per-16 E4M3 scale factors, fa4_pv_mode "bf16"). ---- */
+
+/* Real NVFP4 encoding of a row-major (rows, cols) BF16 matrix, groups of 16
+ * along the contiguous axis; cols must be a multiple of 16. Writes `packed`
+ * (rows * cols / 2 bytes: byte j of a row holds elements 2j (low nibble) and
+ * 2j + 1 (high nibble) as E2M1 codes, sign in bit 3) and `scales` (rows *
+ * cols / 16 E4M3FN bytes, one per group in order). The decoded values are
+ * bit for bit those of attnqat_fake_nvfp4. A group whose scale rounds to 0
+ * gets scale byte 0 and codes 0 or 8 (the element's sign). Device pointers,
+ * 16-byte aligned; the caller owns them. */
+attnqat_status attnqat_nvfp4_pack(const void* x_bf16, void* packed, void* scales, int64_t rows, int64_t cols,
+                                  void* stream);
+
+/* Workspace bytes of attnqat_infer_fwd (0 if the problem is not supported by
+ * it): packed Q and K and their scale factors, each 256-byte aligned. */
+size_t attnqat_infer_fwd_workspace_bytes(const attnqat_problem* p);
+
+/* Inference forward on pre-packed Q and K: O = softmax(softmax_scale *
+ * Q^ K^T) V with Q^, K^ the values q_fp4 / k_fp4 encode (attnqat_nvfp4_pack
+ * layout over (B*H*S, 128): q_fp4 (B, H, Sq, 64) bytes, q_sf (B, H, Sq, 8);
+ * k_fp4, k_sf likewise over Sk) and V BF16 (B, H, Sk, D) unquantized. Writes
+ * o (BF16, (B, H, Sq, D)) and, when lse is not NULL, the natural-log LSE
+ * (FP32, (B, H, Sq)). D must be 128 (ATTNQAT_ERR_UNSUPPORTED otherwise). No
+ * probability quantization and no O': it serves inference only. */
+attnqat_status attnqat_infer_fwd_packed(const attnqat_problem* p, const void* q_fp4, const void* q_sf,
+                                        const void* k_fp4, const void* k_sf, const void* v, void* o, float* lse,
+                                        void* stream);
+
+/* Inference forward from BF16 q, k, v: packs Q and K into the workspace
+ * (attnqat_nvfp4_pack) and runs attnqat_infer_fwd_packed. Needs
+ * attnqat_infer_fwd_workspace_bytes(p) bytes of workspace. */
+attnqat_status attnqat_infer_fwd(const attnqat_problem* p, const void* q, const void* k, const void* v, void* o,
+                                 float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
 /* ---- device status ---- */
 
 /* Synchronizes the current device, then returns ATTNQAT_OK or the first
