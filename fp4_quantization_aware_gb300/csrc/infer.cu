@@ -9,43 +9,54 @@
 // K are exactly fake_nvfp4(Q), fake_nvfp4(K), so O equals the training
 // forward's O' with an unquantized V.
 //
-// One CTA per 128-row query tile of one (b, h). Two passes over the key tiles,
-// so that no accumulator is ever rescaled:
-//   pass 1: S = Q K^T (2 FP4 MMAs of K = 64 per tile), row max only;
-//   pass 2: S again, P = exp2(S * c2 - m) in BF16 written back over S in TMEM,
-//           O += P V (8 BF16 MMAs with A from TMEM), row sum l.
+// One CTA per 128-row query tile of one (b, h), one pass over the key tiles
+// with an online softmax:
+//   S(j) = Q K(j)^T            2 FP4 MMAs (K = 64 each) into TMEM buffer j % 2
+//   m    = running row max; O and l are rescaled only when the tile's max
+//          exceeds the reference by more than kRescaleLog2 (P <= 2^8 otherwise)
+//   P(j) = exp2(S * c2 - m) in BF16, written back over S(j) in TMEM
+//   O   += P(j) V(j)           8 BF16 MMAs with A read from TMEM
 // O = O / l at the end; LSE = (m + log2 l) * ln 2.
+//
+// The softmax work is split over 8 warps: warp w owns lane quarter w % 4 (32
+// query rows) and key half w / 4 (64 of the tile's 128 keys). The two warps of
+// a quarter exchange their half-row maxima through shared memory once per
+// tile (a 64-thread named barrier), so both take the same rescaling decision.
+// Tensor-pipe order: S(0) S(1) PV(0) S(2) PV(1) S(3) ...; tcgen05 MMAs from one
+// thread execute in issue order, so S(j+2) overwrites buffer j % 2 only after
+// PV(j) has read P(j) from it.
 //
 // Block-scaled MMA operands (measured contract): A and B K-major with 64-byte
 // rows (128 E2M1 values, even element in the low nibble) and the 64-byte
 // swizzle, 32 bytes per K = 64 step; scale factors in TMEM, 4 columns per K = 64
-// step, lane r (in every lane quarter) holding in column j the four E4M3 bytes
-// of row r + 32 j; scale-factor column addresses are multiples of 4.
+// step, lane r (in every lane quarter) holding in column c the four E4M3 bytes
+// of row r + 32 c; scale-factor column addresses are multiples of 4.
 //
 // TMEM columns: S0 [0,128), S1 [128,256), O [256,384), Q scales [384,392),
-// K scales x2 [400,408) and [416,424). Warps: 0-3 softmax (thread = query row,
-// all 128 keys of a tile), 4 TMA producer, 5 MMA issuer.
-// Shared memory: Q 8K, K x2 16K, V x2 64K.
+// K scales x2 [400,408) and [416,424). Warps: 0-7 softmax, 8 TMA producer,
+// 9 MMA issuer.
 #include "attn_common.cuh"
 
 namespace attnqat {
 namespace {
 
-constexpr int kThreadsInf = 6 * 32;
-constexpr int kWarpTmaI = 4;
-constexpr int kWarpMmaI = 5;
+constexpr int kWarpTmaI = 8;
+constexpr int kWarpMmaI = 9;
+constexpr int kThreadsInf = 10 * 32;
 constexpr int kD = 128;
+constexpr int kStagesK = 3;
+constexpr int kStagesV = 3;
+constexpr float kRescaleLog2 = 8.0f;
 
 struct InfLayout {
   static constexpr uint32_t kFp4Tile = 128 * 64;          // 128 rows x 64 bytes
   static constexpr uint32_t kVTile = 128 * kD * 2;
   static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kK0 = kQ + kFp4Tile;
-  static constexpr uint32_t kK1 = kK0 + kFp4Tile;
-  static constexpr uint32_t kV0 = kK1 + kFp4Tile;          // 1024-aligned: 24 KiB
-  static constexpr uint32_t kV1 = kV0 + kVTile;
-  static constexpr uint32_t kBar = kV1 + kVTile;
-  static constexpr uint32_t kBytes = kBar + 256;
+  static constexpr uint32_t kK = kQ + kFp4Tile;
+  static constexpr uint32_t kV = kK + kStagesK * kFp4Tile;   // 1024-aligned
+  static constexpr uint32_t kBar = kV + kStagesV * kVTile;
+  static constexpr uint32_t kXchg = kBar + 512;               // maxima, flags [2][2][128], sums [2][128]
+  static constexpr uint32_t kBytes = kXchg + 10 * 128 * 4;
   static constexpr uint32_t kAlloc = kBytes + 1024;
   static constexpr uint32_t kColS0 = 0;
   static constexpr uint32_t kColO = 256;
@@ -53,23 +64,25 @@ struct InfLayout {
   static constexpr uint32_t kColSFK0 = 400;
   static constexpr uint32_t kColSFK1 = 416;
 };
+static_assert(InfLayout::kV % 1024 == 0, "V stages need 1024-byte alignment");
+static_assert(InfLayout::kAlloc <= 227 * 1024, "shared memory");
 
 struct InfBars {
   uint64_t q_full;
-  uint64_t sfq_ready;
-  uint64_t k_full[2];
-  uint64_t k_empty[2];
-  uint64_t v_full[2];
-  uint64_t v_empty[2];
+  uint64_t sf_init;       // Q scales and the K scales of tiles 0 and 1 are in TMEM
+  uint64_t k_full[kStagesK];
+  uint64_t k_empty[kStagesK];
+  uint64_t v_full[kStagesV];
+  uint64_t v_empty[kStagesV];
   uint64_t s_full[2];
-  uint64_t s_free[2];     // pass 1: the softmax warps have read S
-  uint64_t sf_ready[2];   // the K scales of the next tile in this buffer are in TMEM
-  uint64_t p_ready[2];    // pass 2: P (BF16) is in TMEM over S
+  uint64_t p_ready[2];    // P(j) is in TMEM over S(j), and the K scales of tile j + 2
+  uint64_t pv_done;       // one phase per PV(j) (waited only before rescaling O)
   uint64_t o_done;
   uint64_t drain;
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
+static_assert(sizeof(InfBars) <= 512, "barrier area");
 
 struct InfArgs {
   const uint8_t* q_sf;    // (B*H, Sq, 8) E4M3
@@ -113,29 +126,56 @@ __device__ __forceinline__ void umma_nvfp4(uint32_t d_tmem, uint64_t a_desc, uin
       : "memory");
 }
 
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t (&r)[4]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n\t"
+      "tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};\n\t"
       "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
       : "memory");
 }
 
-// Scales of a 128-row tile (rows row0.., `rows` valid) into the 8 TMEM columns
-// at `col` of this warp's lane quarter, in the replicated layout above. Every
-// softmax warp writes the same values into its own quarter.
-__device__ __forceinline__ void write_scales(uint32_t taddr_quarter, const uint8_t* sf, int64_t row0, int rows) {
+// The scale bytes one thread writes for one K = 64 step (`ks`) of a 128-row
+// tile: word c = the four E4M3 scales of groups 4 ks .. 4 ks + 3 of row
+// lane + 32 c (0 past `rows`).
+__device__ __forceinline__ void load_scales(const uint8_t* sf, int64_t row0, int rows, int ks, uint32_t (&w)[4]) {
   const int r = static_cast<int>(lane_id());
-  uint32_t w[8];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int row = r + 32 * j;
-    uint2 v = make_uint2(0u, 0u);
-    if (row < rows) v = __ldg(reinterpret_cast<const uint2*>(sf + (row0 + row) * 8));
-    w[j] = v.x;          // K step 0: groups 0..3
-    w[4 + j] = v.y;      // K step 1: groups 4..7
+  for (int c = 0; c < 4; ++c) {
+    const int row = r + 32 * c;
+    w[c] = row < rows ? __ldg(reinterpret_cast<const uint32_t*>(sf + (row0 + row) * 8 + ks * 4)) : 0u;
   }
-  tmem_st8(taddr_quarter, w);
+}
+
+// Packed FP32 pair arithmetic (two lanes of work per instruction).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(reinterpret_cast<unsigned long long&>(d))
+      : "l"(reinterpret_cast<unsigned long long&>(a)), "l"(reinterpret_cast<unsigned long long&>(b)),
+        "l"(reinterpret_cast<unsigned long long&>(c)));
+  return d;
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  float2 d;
+  asm("add.rn.f32x2 %0, %1, %2;"
+      : "=l"(reinterpret_cast<unsigned long long&>(d))
+      : "l"(reinterpret_cast<unsigned long long&>(a)), "l"(reinterpret_cast<unsigned long long&>(b)));
+  return d;
+}
+
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  float2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;"
+      : "=l"(reinterpret_cast<unsigned long long&>(d))
+      : "l"(reinterpret_cast<unsigned long long&>(a)), "l"(reinterpret_cast<unsigned long long&>(b)));
+  return d;
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 __global__ void __launch_bounds__(kThreadsInf, 1)
@@ -146,24 +186,24 @@ __global__ void __launch_bounds__(kThreadsInf, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   InfBars& B = *reinterpret_cast<InfBars*>(smem + L::kBar);
+  float* xmax = reinterpret_cast<float*>(smem + L::kXchg);        // [slot 2][half 2][row 128]
+  uint32_t* xok = reinterpret_cast<uint32_t*>(xmax + 4 * 128);    // [slot 2][half 2][row 128]
+  float* xsum = xmax + 8 * 128;                                   // [half 2][row 128]
 
   const int warp = warp_id();
   const int lane = lane_id();
   const int i = a.causal ? (a.n_qtiles - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
   const int bh = blockIdx.y;
   const int nk = a.causal ? i + 1 : a.n_ktiles;
-  const int nt = 2 * nk;                     // pass 1: T < nk; pass 2: T >= nk
 
   if (threadIdx.x == 0) {
     B.abort_flag = 0;
     mbar_init(&B.q_full, 1);
-    mbar_init(&B.sfq_ready, 128);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&B.k_full[s], 1), mbar_init(&B.k_empty[s], 1);
-      mbar_init(&B.v_full[s], 1), mbar_init(&B.v_empty[s], 1);
-      mbar_init(&B.s_full[s], 1), mbar_init(&B.s_free[s], 128);
-      mbar_init(&B.sf_ready[s], 128), mbar_init(&B.p_ready[s], 128);
-    }
+    mbar_init(&B.sf_init, 256);
+    for (int s = 0; s < kStagesK; ++s) mbar_init(&B.k_full[s], 1), mbar_init(&B.k_empty[s], 1);
+    for (int s = 0; s < kStagesV; ++s) mbar_init(&B.v_full[s], 1), mbar_init(&B.v_empty[s], 1);
+    for (int s = 0; s < 2; ++s) mbar_init(&B.s_full[s], 1), mbar_init(&B.p_ready[s], 256);
+    mbar_init(&B.pv_done, 1);
     mbar_init(&B.o_done, 1);
     mbar_init(&B.drain, 1);
     fence_mbar_init();
@@ -182,30 +222,36 @@ __global__ void __launch_bounds__(kThreadsInf, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q), tma_prefetch_desc(&tm_k), tma_prefetch_desc(&tm_v);
-      int k_uses[2] = {0, 0}, v_uses[2] = {0, 0};
+      int k_uses[kStagesK] = {}, v_uses[kStagesV] = {};
+      auto load_k = [&](int j) -> bool {
+        const int s = j % kStagesK;
+        if (j >= kStagesK && !mbar_wait(&B.k_empty[s], ((j / kStagesK) - 1) & 1, ctl)) return false;
+        mbar_arrive_expect_tx(&B.k_full[s], L::kFp4Tile);
+        tma_load_3d(smem + L::kK + s * L::kFp4Tile, &tm_k, &B.k_full[s], 0, j * 128, bh);
+        ++k_uses[s];
+        return true;
+      };
+      auto load_v = [&](int j) -> bool {
+        const int s = j % kStagesV;
+        if (j >= kStagesV && !mbar_wait(&B.v_empty[s], ((j / kStagesV) - 1) & 1, ctl)) return false;
+        mbar_arrive_expect_tx(&B.v_full[s], L::kVTile);
+        for (int b = 0; b < kD / 64; ++b)
+          tma_load_3d(smem + L::kV + s * L::kVTile + b * kBlockBytes, &tm_v, &B.v_full[s], b * 64, j * 128, bh);
+        ++v_uses[s];
+        return true;
+      };
       mbar_arrive_expect_tx(&B.q_full, L::kFp4Tile);
       tma_load_3d(smem + L::kQ, &tm_q, &B.q_full, 0, i * 128, bh);
-      for (int T = 0; T < nt; ++T) {
-        const int jt = T < nk ? T : T - nk;
-        const int s = T & 1;
-        if (T >= 2 && !mbar_wait(&B.k_empty[s], ((T >> 1) - 1) & 1, ctl)) break;
-        mbar_arrive_expect_tx(&B.k_full[s], L::kFp4Tile);
-        tma_load_3d(smem + (s ? L::kK1 : L::kK0), &tm_k, &B.k_full[s], 0, jt * 128, bh);
-        ++k_uses[s];
-        if (T >= nk) {
-          const int tv = T - nk, sv = tv & 1;
-          if (tv >= 2 && !mbar_wait(&B.v_empty[sv], ((tv >> 1) - 1) & 1, ctl)) break;
-          mbar_arrive_expect_tx(&B.v_full[sv], L::kVTile);
-          for (int b = 0; b < kD / 64; ++b)
-            tma_load_3d(smem + (sv ? L::kV1 : L::kV0) + b * kBlockBytes, &tm_v, &B.v_full[sv], b * 64, jt * 128, bh);
-          ++v_uses[sv];
-        }
+      bool ok = load_k(0);
+      for (int j = 0; ok && j < nk; ++j) {
+        if (j + 1 < nk) ok = load_k(j + 1);
+        if (ok) ok = load_v(j);
       }
       mbar_wait_drain(&B.q_full, 0, ctl);
-      for (int s = 0; s < 2; ++s) {
+      for (int s = 0; s < kStagesK; ++s)
         if (k_uses[s]) mbar_wait_drain(&B.k_full[s], (k_uses[s] - 1) & 1, ctl);
+      for (int s = 0; s < kStagesV; ++s)
         if (v_uses[s]) mbar_wait_drain(&B.v_full[s], (v_uses[s] - 1) & 1, ctl);
-      }
     }
   } else if (warp == kWarpMmaI) {
     // ------------------------------------------------------------ MMA issuer
@@ -214,137 +260,171 @@ __global__ void __launch_bounds__(kThreadsInf, 1)
       constexpr uint32_t kIdO = idesc_bf16(128, kD, false, true);
       const uint64_t dq = sdesc_sw64(sbase + L::kQ);
       const uint64_t mnmaj = sdesc_sw128(sbase, kBlockBytes, 1024);
-      auto issue_s = [&](int T) -> bool {
-        const int s = T & 1;
-        if (!mbar_wait(&B.k_full[s], (T >> 1) & 1, ctl)) return false;
-        // previous occupant of this S buffer: read by the softmax warps (pass 1),
-        // or its P read by the PV MMA issued earlier by this thread (in order)
-        const int u = T - 2;
-        if (u >= 0 && u < nk && !mbar_wait(&B.s_free[s], (u >> 1) & 1, ctl)) return false;
-        if (!mbar_wait(&B.sf_ready[s], (T >> 1) & 1, ctl)) return false;
+      auto issue_s = [&](int j) -> bool {
+        const int s = j % kStagesK, b = j & 1;
+        if (!mbar_wait(&B.k_full[s], (j / kStagesK) & 1, ctl)) return false;
         tc_fence_after();
-        const uint64_t dk = sdesc_sw64(sbase + (s ? L::kK1 : L::kK0));
-        const uint32_t sfk = s ? L::kColSFK1 : L::kColSFK0;
+        const uint64_t dk = sdesc_sw64(sbase + L::kK + s * L::kFp4Tile);
+        const uint32_t sfk = b ? L::kColSFK1 : L::kColSFK0;
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks)
-          umma_nvfp4(tmem + L::kColS0 + s * 128, sdesc_advance(dq, ks * 32), sdesc_advance(dk, ks * 32), kIdS,
+          umma_nvfp4(tmem + L::kColS0 + b * 128, sdesc_advance(dq, ks * 32), sdesc_advance(dk, ks * 32), kIdS,
                      tmem + L::kColSFQ + ks * 4, tmem + sfk + ks * 4, ks > 0);
-        umma_commit(&B.s_full[s]);
+        umma_commit(&B.s_full[b]);
         umma_commit(&B.k_empty[s]);
         return true;
       };
-      bool ok = mbar_wait(&B.q_full, 0, ctl) && mbar_wait(&B.sfq_ready, 0, ctl) && issue_s(0);
-      for (int T = 0; ok && T < nt; ++T) {
-        if (T + 1 < nt && !issue_s(T + 1)) break;
-        if (T >= nk) {
-          const int tv = T - nk, sv = tv & 1;
-          if (!mbar_wait(&B.v_full[sv], (tv >> 1) & 1, ctl)) break;
-          const int pr_use = (T >> 1) - ((nk + 1 - (T & 1)) >> 1);
-          if (!mbar_wait(&B.p_ready[T & 1], pr_use & 1, ctl)) break;
-          tc_fence_after();
-          const uint64_t dv = sdesc_advance(mnmaj, sv ? L::kV1 : L::kV0);
-          const uint32_t pc = L::kColS0 + (T & 1) * 128;    // P: keys 2c, 2c+1 in column pc + c
+      bool ok = mbar_wait(&B.q_full, 0, ctl) && mbar_wait(&B.sf_init, 0, ctl) && issue_s(0) &&
+                (nk < 2 || issue_s(1));
+      for (int j = 0; ok && j < nk; ++j) {
+        const int sv = j % kStagesV, b = j & 1;
+        if (!mbar_wait(&B.v_full[sv], (j / kStagesV) & 1, ctl)) break;
+        if (!mbar_wait(&B.p_ready[b], (j >> 1) & 1, ctl)) break;
+        tc_fence_after();
+        const uint64_t dv = sdesc_advance(mnmaj, L::kV + sv * L::kVTile);
+        const uint32_t pc = L::kColS0 + b * 128;   // keys 64h + 2c, +1 of P in column pc + 64h + c
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_bf16_tmem_a(tmem + L::kColO, tmem + pc + kk * 8, sdesc_advance(dv, kk * 2048), kIdO,
-                             (tv > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(&B.v_empty[sv]);
-          if (tv == nk - 1) umma_commit(&B.o_done);
-        }
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16_tmem_a(tmem + L::kColO, tmem + pc + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_advance(dv, kk * 2048),
+                           kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&B.v_empty[sv]);
+        umma_commit(&B.pv_done);
+        if (j == nk - 1) umma_commit(&B.o_done);
+        if (j + 2 < nk && !issue_s(j + 2)) break;
       }
       umma_commit(&B.drain);
       mbar_wait_drain(&B.drain, 0, ctl);
     }
   } else {
-    // ------------------------------------------------------------ softmax (warps 0-3)
-    const uint32_t quarter = warp;
+    // ------------------------------------------------------------ softmax (warps 0-7)
+    const uint32_t quarter = warp & 3, half = warp >> 2;
     const uint32_t r = quarter * 32 + lane;
     const uint32_t lane_off = (quarter * 32u) << 16;
+    const uint32_t bar_id = 1 + quarter;                          // the quarter's two warps
     const int qrow = i * 128 + static_cast<int>(r);
     const int kend = a.causal ? min(a.Sk, qrow + 1) : a.Sk;
     const int64_t qbase = static_cast<int64_t>(bh) * a.Sq, kbase = static_cast<int64_t>(bh) * a.Sk;
-    bool ok = true;
-    auto k_scales = [&](int T) {   // K scales of global tile T into its buffer
-      const int jt = T < nk ? T : T - nk;
-      write_scales(tmem + lane_off + ((T & 1) ? L::kColSFK1 : L::kColSFK0), a.k_sf, kbase + jt * 128,
-                   min(128, a.Sk - jt * 128));
+    {
+      uint32_t w[4];
+      load_scales(a.q_sf, qbase + i * 128, min(128, a.Sq - i * 128), half, w);
+      tmem_st4(tmem + lane_off + L::kColSFQ + 4 * half, w);
+      load_scales(a.k_sf, kbase, min(128, a.Sk), half, w);
+      tmem_st4(tmem + lane_off + L::kColSFK0 + 4 * half, w);
+      if (nk > 1) {
+        load_scales(a.k_sf, kbase + 128, min(128, a.Sk - 128), half, w);
+        tmem_st4(tmem + lane_off + L::kColSFK1 + 4 * half, w);
+      }
       tc_fence_before();
-      mbar_arrive(&B.sf_ready[T & 1]);
-    };
-    write_scales(tmem + lane_off + L::kColSFQ, a.q_sf, qbase + i * 128, min(128, a.Sq - i * 128));
-    tc_fence_before();
-    mbar_arrive(&B.sfq_ready);
-    k_scales(0);
-    if (nt > 1) k_scales(1);
+      mbar_arrive(&B.sf_init);
+    }
 
-    // pass 1: row max of S * c2
-    float m = -INFINITY;
-    for (int T = 0; T < nk; ++T) {
-      const int s = T & 1;
-      const int valid = kend - T * 128;
-      if (!warp_wait(&B.s_full[s], (T >> 1) & 1, ctl)) { ok = false; break; }
-      tc_fence_after();
-      float mc[4] = {m, m, m, m};
+    float mref = -INFINITY;                    // reference max, in exp2 units
+    float2 acc0 = make_float2(0.0f, 0.0f), acc1 = make_float2(0.0f, 0.0f);
+    bool ok = true, fail = false;
+    for (int j = 0; j < nk; ++j) {
+      const int b = j & 1;
+      const bool more = j + 2 < nk;
+      uint32_t sfw[4] = {0u, 0u, 0u, 0u};
+      if (more) load_scales(a.k_sf, kbase + (j + 2) * 128, min(128, a.Sk - (j + 2) * 128), half, sfw);
+      const uint32_t scol = tmem + lane_off + L::kColS0 + b * 128 + 64 * half;
+      uint32_t v[64];
+      const bool got = !fail && warp_wait(&B.s_full[b], (j >> 1) & 1, ctl);
+      if (got) {
+        tc_fence_after();
+        tmem_ld64(scol, v);
+      } else {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t v[64];
-        tmem_ld64(tmem + lane_off + L::kColS0 + s * 128 + h * 64, v);
+        for (int k = 0; k < 64; ++k) v[k] = 0u;
+      }
+      const int valid = kend - j * 128 - 64 * static_cast<int>(half);
+      if (valid < 64) {
 #pragma unroll
         for (int k = 0; k < 64; ++k)
-          if (h * 64 + k < valid) mc[k & 3] = fmaxf(mc[k & 3], __uint_as_float(v[k]) * a.c2);
+          if (k >= valid) v[k] = __float_as_uint(-INFINITY);
       }
-      tc_fence_before();
-      mbar_arrive(&B.s_free[s]);
-      m = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3]));
-      if (T + 2 < nt) k_scales(T + 2);
-    }
-    if (m == -INFINITY) m = 0.0f;   // a row with no live key (not reached for rows < Sq)
-
-    // pass 2: P = exp2(S * c2 - m) as BF16 over S; row sum
-    float lc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    for (int T = nk; ok && T < nt; ++T) {
-      const int s = T & 1, tv = T - nk;
-      const int valid = kend - tv * 128;
-      if (!warp_wait(&B.s_full[s], (T >> 1) & 1, ctl)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t scol = tmem + lane_off + L::kColS0 + s * 128;
-      uint32_t pw[64];
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t v[64];
-        tmem_ld64(scol + h * 64, v);
+      for (int k = 0; k < 64; k += 8) {
+        mx[0] = fmax3(mx[0], __uint_as_float(v[k]), __uint_as_float(v[k + 1]));
+        mx[1] = fmax3(mx[1], __uint_as_float(v[k + 2]), __uint_as_float(v[k + 3]));
+        mx[2] = fmax3(mx[2], __uint_as_float(v[k + 4]), __uint_as_float(v[k + 5]));
+        mx[3] = fmax3(mx[3], __uint_as_float(v[k + 6]), __uint_as_float(v[k + 7]));
+      }
+      // half-row maxima and health flags through shared memory (both warps
+      // of the quarter always reach this barrier the same number of times)
+      const int slot = (j & 1) * 2;
+      xmax[(slot + half) * 128 + r] = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+      xok[(slot + half) * 128 + r] = got ? 1u : 0u;
+      named_bar_sync(bar_id, 64);
+      const float tmax = fmaxf(xmax[(slot + half) * 128 + r], xmax[(slot + (half ^ 1)) * 128 + r]);
+      if (!got || xok[(slot + (half ^ 1)) * 128 + r] == 0u) {
+        ok = false;
+        break;
+      }
+      const float ms = tmax * a.c2;
+      // The rescaling decision is per row, but the wait and the TMEM accesses
+      // below are warp-collective: the whole warp enters when any of its rows
+      // needs it (rows that do not use the factor 1). Both warps of a quarter
+      // hold the same rows, so they take the same branch.
+      const bool need = j > 0 && ms > mref + kRescaleLog2;
+      if (j == 0) mref = ms;
+      if (__any_sync(0xffffffffu, need)) {
+        const float f = need ? ex2(mref - ms) : 1.0f;
+        if (need) mref = ms;
+        const float2 f2 = make_float2(f, f);
+        acc0 = fmul2(acc0, f2), acc1 = fmul2(acc1, f2);
+        // O holds PV(0..j-1): wait for PV(j-1), then rescale this half's columns
+        if (warp_wait(&B.pv_done, (j - 1) & 1, ctl)) {
+          tc_fence_after();
+          uint32_t o[32];
 #pragma unroll
-        for (int k = 0; k < 64; k += 2) {
-          const float p0 = (h * 64 + k < valid) ? ex2(fmaf(__uint_as_float(v[k]), a.c2, -m)) : 0.0f;
-          const float p1 = (h * 64 + k + 1 < valid) ? ex2(fmaf(__uint_as_float(v[k + 1]), a.c2, -m)) : 0.0f;
-          lc[k & 3] += p0;
-          lc[(k + 1) & 3] += p1;
-          pw[h * 32 + k / 2] = pack_bf16x2(p0, p1);
+          for (int c = 0; c < 2; ++c) {
+            const uint32_t oc = tmem + lane_off + L::kColO + 64 * half + 32 * c;
+            tmem_ld32(oc, o);
+#pragma unroll
+            for (int k = 0; k < 32; k += 2) {
+              const float2 t = fmul2(make_float2(__uint_as_float(o[k]), __uint_as_float(o[k + 1])), f2);
+              o[k] = __float_as_uint(t.x), o[k + 1] = __float_as_uint(t.y);
+            }
+            tmem_st32(oc, o);
+          }
+        } else {
+          fail = true;
         }
       }
-      uint32_t half0[32], half1[32];
+      const float2 c2v = make_float2(a.c2, a.c2), nm = make_float2(-mref, -mref);
+      uint32_t pw[32];
 #pragma unroll
-      for (int k = 0; k < 32; ++k) half0[k] = pw[k], half1[k] = pw[32 + k];
-      tmem_st32(scol, half0);          // keys 0..63 in columns 0..31
-      tmem_st32(scol + 32, half1);     // keys 64..127 in columns 32..63
-      tc_fence_before();
-      mbar_arrive(&B.p_ready[s]);
-      if (T + 2 < nt) k_scales(T + 2);
-    }
-    const float l = (lc[0] + lc[1]) + (lc[2] + lc[3]);
-
-    // epilogue: O / l, LSE
-    if (ok && warp_wait(&B.o_done, 0, ctl)) {
-      tc_fence_after();
-      const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-      bf16* out = a.o + (qbase + qrow) * kD;
-#pragma unroll
-      for (int c = 0; c < kD / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_off + L::kColO + c * 32, v);
-        if (qrow < a.Sq) store_row32_bf16(out + c * 32, v, inv);
+      for (int c = 0; c < 32; ++c) {
+        const float2 x = ffma2(make_float2(__uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1])), c2v, nm);
+        const float2 p = make_float2(ex2(x.x), ex2(x.y));
+        if (c & 1) acc1 = fadd2(acc1, p);
+        else acc0 = fadd2(acc0, p);
+        pw[c] = pack_bf16x2(p.x, p.y);
       }
-      if (a.lse != nullptr && qrow < a.Sq) a.lse[qbase + qrow] = (m + lg2(l)) * kLn2;
+      tmem_st32(scol, pw);                                   // over this warp's own S columns
+      if (more) tmem_st4(tmem + lane_off + (b ? L::kColSFK1 : L::kColSFK0) + 4 * half, sfw);
+      tc_fence_before();
+      mbar_arrive(&B.p_ready[b]);
+    }
+    const float2 lt = fadd2(acc0, acc1);
+    const float l = lt.x + lt.y;
+    xsum[half * 128 + r] = l;
+    named_bar_sync(bar_id, 64);
+    const float ltot = l + xsum[(half ^ 1) * 128 + r];
+
+    // epilogue: this half's 64 columns of O / l; LSE
+    if (ok && !fail && warp_wait(&B.o_done, 0, ctl)) {
+      tc_fence_after();
+      const float inv = ltot > 0.0f ? 1.0f / ltot : 0.0f;
+      bf16* out = a.o + (qbase + qrow) * kD + 64 * half;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tmem + lane_off + L::kColO + 64 * half + 32 * c, o);
+        if (qrow < a.Sq) store_row32_bf16(out + 32 * c, o, inv);
+      }
+      if (half == 0 && a.lse != nullptr && qrow < a.Sq) a.lse[qbase + qrow] = (mref + lg2(ltot)) * kLn2;
     }
   }
 
