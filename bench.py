@@ -17,6 +17,12 @@ the float64 CPU oracle on whole heads of the same workload (about 10 s).
 With --gpus N (launched by torchrun) every rank runs the full workload on its
 own GPU (independent problems, no collective on the data path) and `value` is
 the sum over ranks divided by the slowest rank's time (weak scaling).
+
+--workload ctx32k (or --path infer) measures the NVFP4 inference forward
+instead: a step is NVFP4 packing of Q and K plus the block-scaled FP4 QK /
+BF16 PV attention kernel (O and LSE), 4*B*H*Sq*Sk*D FLOPs (halved for
+causal). Its roofline is the exp2 (MUFU) bound of the softmax, with the
+tensor-pipe bound beside it.
 """
 from __future__ import annotations
 
@@ -43,6 +49,15 @@ KERNEL_SOURCES = [os.path.join(ROOT, "fp4_quantization_aware_gb300", "csrc", f)
 
 
 METRIC = "QAT attn bwd TFLOP/s on 1 GB300 (fwd in fwd_tflops); % of dense BF16 peak in roofline"
+METRIC_INFER = "NVFP4 inference attn fwd TFLOP/s on 1 GB300 (pack Q/K + FP4 QK / BF16 PV kernel)"
+INFER_SOURCES = [os.path.join(ROOT, "fp4_quantization_aware_gb300", "csrc", f)
+                 for f in ("infer.cu", "attn_common.cuh", "nvfp4.cuh", "ptx.cuh")]
+PROFILE_INFER_JSON = os.path.join(ROOT, "profiles", "infer_kernel_ctx32k_counters.json")
+# exp2 results per clock per SM of the MUFU unit (ex2.approx), as measured on
+# this GPU by a throughput probe (16 lanes x 4 sub-partitions x 2 on the
+# Blackwell Ultra SFU, whose exp throughput is twice Blackwell's).
+MUFU_EX2_PER_CLK_SM = 32
+FP4_OVER_BF16 = 6.0        # nominal dense FP4 / BF16 tensor ratio of GB300 (13.5 / 2.25 PFLOP/s)
 
 
 def max_over_ranks(values, device=None):
@@ -63,9 +78,9 @@ def job_tflops(flops_per_rank_step: float, steps: int, world: int, max_ms: float
     return world * flops_per_rank_step * steps / (max_ms * 1e-3) / 1e12
 
 
-def kernel_hash() -> str:
+def kernel_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in (sources or KERNEL_SOURCES):
         h.update(open(f, "rb").read())
     return h.hexdigest()[:16]
 
@@ -233,6 +248,161 @@ def run_ours(args, w, rank, world, local_rank):
     return res
 
 
+def run_infer(args, w, rank, world, local_rank):
+    """Time the NVFP4 inference forward (pack Q, pack K, attention kernel)."""
+    import torch
+    from fp4_quantization_aware_gb300 import attnqat
+    import ctypes
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    lib = attnqat.load()
+    x = synth.inputs(w)
+    t = {n: torch.from_numpy(x[n]).to(torch.bfloat16).to(dev) for n in ("q", "k", "v")}
+    del x
+    p = attnqat.problem(w.B, w.H, w.Sq, w.Sk, w.D, w.causal, w.scale)
+    pp = ctypes.byref(p)
+    need = lib.attnqat_infer_fwd_workspace_bytes(pp)
+    if need == 0:
+        attnqat.check(lib.attnqat_check_support(pp), "check_support")
+        raise SystemExit("the inference forward needs D == 128")
+    bh = w.B * w.H
+    qp = torch.empty(bh * w.Sq * 64, dtype=torch.uint8, device=dev)
+    qs = torch.empty(bh * w.Sq * 8, dtype=torch.uint8, device=dev)
+    kp = torch.empty(bh * w.Sk * 64, dtype=torch.uint8, device=dev)
+    ks = torch.empty(bh * w.Sk * 8, dtype=torch.uint8, device=dev)
+    ws = attnqat.workspace(need, dev)
+    o = torch.empty_like(t["q"])
+    lse = torch.empty(w.shape_q[:3], dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    P = lambda a: a.data_ptr()  # noqa: E731
+
+    def step(ev=None):
+        attnqat.check(lib.attnqat_nvfp4_pack(P(t["q"]), P(qp), P(qs), bh * w.Sq, w.D, sp), "pack q")
+        attnqat.check(lib.attnqat_nvfp4_pack(P(t["k"]), P(kp), P(ks), bh * w.Sk, w.D, sp), "pack k")
+        if ev:
+            ev[0].record(stream)
+        attnqat.check(lib.attnqat_infer_fwd_packed(pp, P(qp), P(qs), P(kp), P(ks), P(t["v"]), P(o), P(lse), sp),
+                      "infer")
+        if ev:
+            ev[1].record(stream)
+
+    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    evs = [(E(), E(), E(), E()) for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clk:
+        torch.cuda.synchronize()
+        for e in evs:
+            flush.zero_()
+            e[0].record(stream)
+            step(ev=(e[1], e[2]))
+            e[3].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    step_ms = sum(e[0].elapsed_time(e[3]) for e in evs) / args.steps
+    kern_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    assert attnqat.device_status() == 0, "a device wait timed out during the bench"
+
+    # end to end: pinned host Q, K, V in, O and LSE out, through attnqat_infer_fwd
+    host_in = {n: t[n].cpu().pin_memory() for n in ("q", "k", "v")}
+    dev_in = {n: torch.empty_like(v, device=dev) for n, v in host_in.items()}
+    host_out = [torch.empty_like(a, device="cpu").pin_memory() for a in (o, lse)]
+    e2e_evs = [(E(), E()) for _ in range(args.steps)]
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        if i >= args.warmup:
+            e2e_evs[i - args.warmup][0].record(stream)
+        for n in dev_in:
+            dev_in[n].copy_(host_in[n], non_blocking=True)
+        attnqat.check(lib.attnqat_infer_fwd(pp, P(dev_in["q"]), P(dev_in["k"]), P(dev_in["v"]), P(o), P(lse), P(ws),
+                                            ws.numel(), sp), "infer e2e")
+        for h, d in zip(host_out, (o, lse)):
+            h.copy_(d, non_blocking=True)
+        if i >= args.warmup:
+            e2e_evs[i - args.warmup][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_evs) / args.steps
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out)
+    res = {"step_ms": step_ms, "kern_ms": kern_ms, "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h,
+           "launches": 3 * args.steps, "clocks": clk.summary()}
+    res["step_ms"], res["e2e_ms"] = max_over_ranks([step_ms, e2e_ms], dev)
+    return res
+
+
+def infer_line(args, w, world, r, peaks, l2) -> dict:
+    flops = w.fwd_flops()
+    kern_ms = statistics.mean(r["kern_ms"])
+    exps = w.B * w.H * w.Sq * w.Sk / (2 if w.causal else 1)
+    sm_mhz = 2070.0
+    mufu_peak = MUFU_EX2_PER_CLK_SM * 152 * sm_mhz * 1e6 / 1e9            # G exp2/s at the maximum SM clock
+    achieved = exps / (kern_ms * 1e-3) / 1e9
+    # tensor-pipe bound: half the FLOPs (QK) at the FP4 rate, half (PV) at the BF16 rate
+    tensor_peak = 2.0 / (1.0 / peaks["bf16"] + 1.0 / (FP4_OVER_BF16 * peaks["bf16"]))
+    tensor_achieved = flops / (kern_ms * 1e-3) / 1e12
+    traffic = None
+    if os.path.exists(PROFILE_INFER_JSON):
+        prof = json.load(open(PROFILE_INFER_JSON))
+        if prof.get("kernel_hash") == kernel_hash(INFER_SOURCES) and prof.get("workload") == w.name:
+            traffic = prof.get("dram_bytes_per_launch")
+    cfg = workload_config(w, l2)
+    cfg["step"] = "NVFP4 pack of Q and K, then the FP4 QK / BF16 PV attention kernel (O, LSE)"
+    return {
+        "metric": METRIC_INFER, "value": job_tflops(flops, 1, world, r["step_ms"]), "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["step_ms"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4 QK, bf16 PV, f32 softmax",
+        "data": "synthetic", "config": cfg,
+        "kernel_tflops": tensor_achieved, "kernel_ms": kern_ms,
+        "roofline": {"bound": "alu", "kernel": "infer_kernel (attnqat_infer_fwd_packed)", "achieved": achieved,
+                     "peak": mufu_peak, "unit": "Gexp2/s", "frac": achieved / mufu_peak, "traffic": traffic,
+                     "launch_ms": kern_ms,
+                     "peak_note": f"MUFU ex2: {MUFU_EX2_PER_CLK_SM}/clk/SM x 152 SMs x {sm_mhz:.0f} MHz (derived)",
+                     "tensor": {"achieved": tensor_achieved, "peak": tensor_peak, "unit": "TFLOP/s",
+                                "frac": tensor_achieved / tensor_peak,
+                                "note": f"QK at {FP4_OVER_BF16:g}x and PV at 1x the {peaks['src']} BF16 peak "
+                                        f"{peaks['bf16']}"}},
+        "e2e": {"value": world * flops / (r["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms": r["e2e_ms"],
+                "what": "attnqat_infer_fwd with pinned host Q, K, V in and O, LSE out"},
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+    }
+
+
+def infer_oracle_rows(w, budget_s):
+    """Time the float64 oracle's inference forward on growing query-row blocks
+    of head (0, 0) until about budget_s; returns (seconds, flops, rows)."""
+    import oracle
+    x = synth.head_inputs(w, 0, 0)
+    rows, flops = 0, 0.0
+    blk = 256
+    t0 = time.perf_counter()
+    kh = oracle.fake_nvfp4(x["k"].astype(np.float64))          # K once per head
+    vv = x["v"].astype(np.float64)
+    spent = time.perf_counter() - t0
+    while spent < budget_s and rows < w.Sq:
+        r1 = min(w.Sq, rows + blk)
+        t0 = time.perf_counter()
+        # fwd_rows slices rows [rows, r1) of its first argument (the causal mask
+        # needs the absolute row index)
+        qh = np.zeros((r1, w.D))
+        qh[rows:r1] = oracle.fake_nvfp4(x["q"][rows:r1].astype(np.float64))
+        oracle.fwd_rows(qh, kh, vv, w.scale, w.causal, rows, r1, quantize=False)
+        spent += time.perf_counter() - t0
+        keys = np.minimum(np.arange(rows, r1) + 1, w.Sk).sum() if w.causal else (r1 - rows) * w.Sk
+        flops += 4.0 * keys * w.D
+        rows = r1
+    return spent, flops, rows
+
+
 # ---------------------------------------------------------------------------- CPU oracle
 def oracle_heads(w, heads):
     """Time the float64 CPU oracle's forward and backward on the listed heads."""
@@ -278,13 +448,45 @@ def main():
     ap.add_argument("--workload", default="c2", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", default=None, choices=["qat", "infer"],
+                    help="qat: the QAT forward+backward step; infer: the NVFP4 inference forward "
+                         "(default: infer for ctx32k, qat otherwise)")
+    ap.add_argument("--seq", type=int, default=None, help="override Sq = Sk of the workload (smaller captures)")
     args = ap.parse_args()
-    w = synth.workload(args.workload)
+    w = synth.workload(args.workload) if args.seq is None else synth.workload(args.workload, Sq=args.seq,
+                                                                               Sk=args.seq)
+    path = args.path or ("infer" if args.workload == "ctx32k" else "qat")
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     peaks = measured_peaks()
     l2 = "flushed: 256 MiB write between steps"
+
+    if args.impl == "reference" and path == "infer":
+        if rank != 0:
+            return
+        t0 = time.perf_counter()
+        per = []
+        for _ in range(args.warmup + args.steps):
+            per.append(infer_oracle_rows(w, 5.0))
+        per = per[args.warmup:]
+        val = sum(f for _, f, _ in per) / sum(s_ for s_, _, _ in per) / 1e12
+        rows = per[0][2]
+        sample = (f"query rows [0, {rows}) of head (b=0, h=0) of {w.B * w.H} per step against all {w.Sk} keys, "
+                  "float64 NumPy")
+        cfg = workload_config(w, l2)
+        cfg["step"] = "NVFP4 pack of Q and K, then the FP4 QK / BF16 PV attention kernel (O, LSE)"
+        print(json.dumps({"impl": "reference", "metric": METRIC_INFER, "value": val, "unit": "TFLOP/s",
+                          "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                          "ms_per_step": 1e3 * sum(s_ for s_, _, _ in per) / args.steps,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                          "data": "synthetic", "config": cfg,
+                          "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": os.cpu_count(),
+                                           "kind": "oracle", "sample": sample},
+                          "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0},
+                          "wall_s": time.perf_counter() - t0}))
+        return
 
     if args.impl == "reference":
         if rank != 0:
@@ -312,6 +514,22 @@ def main():
     import torch
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    if path == "infer":
+        r = run_infer(args, w, rank, world, local_rank)
+        if rank != 0:
+            torch.distributed.destroy_process_group()
+            return
+        line = infer_line(args, w, world, r, peaks, l2)
+        if not args.no_cpu_baseline and world == 1:
+            secs, fl, rows = infer_oracle_rows(w, 10.0)
+            line["cpu_baseline"] = {"value": fl / secs / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
+                                    "kind": "oracle",
+                                    "sample": f"query rows [0, {rows}) of head (0, 0) against all {w.Sk} keys: "
+                                              f"{secs:.2f} s, float64 NumPy (BLAS on all cores)"}
+        print(json.dumps(line))
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
     r = run_ours(args, w, rank, world, local_rank)
     if rank != 0:
         torch.distributed.destroy_process_group()
