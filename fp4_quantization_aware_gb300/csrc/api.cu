@@ -36,8 +36,12 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsLayout {
-  size_t qh, kh, vh, delta, dq_acc, total;
+  size_t qh, kh, vh, delta, dq_acc, split, split_slots, total;
 };
+
+Problem to_problem(const attnqat_problem& p) {
+  return Problem{p.B, p.H, p.Sq, p.Sk, p.D, p.is_causal != 0, p.softmax_scale};
+}
 
 WsLayout layout(const attnqat_problem& p, bool bwd) {
   const size_t bh = static_cast<size_t>(p.B) * p.H;
@@ -49,6 +53,11 @@ WsLayout layout(const attnqat_problem& p, bool bwd) {
   if (bwd) {
     w.delta = off, off += round256(bh * p.Sq * 4);
     w.dq_acc = off, off += round256(bh * p.Sq * p.D * 4);
+    // split key tiles of the backward: counters, then FP32 [dK, dV] slots
+    const int64_t tiles = ((p.Sk + kBlockN - 1) / kBlockN) * static_cast<int64_t>(bh);
+    w.split_slots = static_cast<size_t>(tiles < kMaxSplitTiles ? tiles : kMaxSplitTiles);
+    w.split = off,
+    off += round256((split_cnt_words() + w.split_slots * split_slot_floats(to_problem(p))) * 4);
   }
   w.total = off;
   return w;
@@ -67,10 +76,6 @@ attnqat_status check_problem(const attnqat_problem* p) {
     return fail(ATTNQAT_ERR_UNSUPPORTED, "sequence length beyond 2^31");
   if (p->B * p->H > 65535) return fail(ATTNQAT_ERR_UNSUPPORTED, "B*H above 65535");
   return ATTNQAT_OK;
-}
-
-Problem to_problem(const attnqat_problem& p) {
-  return Problem{p.B, p.H, p.Sq, p.Sk, p.D, p.is_causal != 0, p.softmax_scale};
 }
 
 attnqat_status check_ptrs(std::initializer_list<const void*> ptrs) {
@@ -236,7 +241,7 @@ attnqat_status attnqat_quantize_qkv(const attnqat_problem* p, const void* q, con
   ATTNQAT_TRY(check_ws(ws, ws_bytes, w.total));
   ATTNQAT_CUDA(launch_prep(to_problem(*p), static_cast<const bf16*>(q), static_cast<const bf16*>(k),
                            static_cast<const bf16*>(v), nullptr, nullptr, at<bf16>(ws, w.qh), at<bf16>(ws, w.kh),
-                           at<bf16>(ws, w.vh), nullptr, nullptr, static_cast<cudaStream_t>(stream)),
+                           at<bf16>(ws, w.vh), nullptr, nullptr, nullptr, 0, static_cast<cudaStream_t>(stream)),
                "quantize_qkv");
   return ATTNQAT_OK;
 }
@@ -275,6 +280,9 @@ attnqat_status attnqat_bwd_preprocess(const attnqat_problem* p, const void* dout
                            static_cast<const bf16*>(v), static_cast<const bf16*>(o_hp),
                            static_cast<const bf16*>(dout), at<bf16>(ws, w.qh), at<bf16>(ws, w.kh),
                            at<bf16>(ws, w.vh), at<float>(ws, w.delta), at<float>(ws, w.dq_acc),
+                           at<float>(ws, w.split),
+                           split_cnt_words() + bwd_split_plan(to_problem(*p), device_sm_count()).n_split *
+                                                   split_slot_floats(to_problem(*p)),
                            static_cast<cudaStream_t>(stream)),
                "bwd_preprocess");
   return ATTNQAT_OK;
@@ -291,7 +299,8 @@ attnqat_status attnqat_bwd_main(const attnqat_problem* p, const void* dout, cons
   if (!err) return st;
   ATTNQAT_CUDA(launch_bwd(to_problem(*p), at<bf16>(ws, w.qh), at<bf16>(ws, w.kh), at<bf16>(ws, w.vh),
                           static_cast<const bf16*>(dout), lse, at<float>(ws, w.delta), at<float>(ws, w.dq_acc),
-                          static_cast<bf16*>(dk), static_cast<bf16*>(dv), err, static_cast<cudaStream_t>(stream)),
+                          static_cast<bf16*>(dk), static_cast<bf16*>(dv), at<float>(ws, w.split) + split_cnt_words(),
+                          at<uint32_t>(ws, w.split), err, static_cast<cudaStream_t>(stream)),
                "bwd_main");
   return ATTNQAT_OK;
 }

@@ -9,7 +9,11 @@
 //
 // One CTA owns a 128-key tile of one (b, h) and walks the 128-row query tiles
 // (causal: from the diagonal tile on, keeping the element mask on the
-// diagonal; tiles past Sq/Sk are zero-filled by TMA and masked).
+// diagonal; tiles past Sq/Sk are zero-filled by TMA and masked). The last
+// n_split key tiles of the grid are each shared by two CTAs, one per half of
+// the query tiles, so that a partial last wave of CTAs runs half as long
+// (bwd_split_plan). Both add their FP32 partial dK, dV rows into a zeroed
+// workspace slot; the one that counts second stores the BF16 sums.
 //
 // Per query tile i (all MMAs tcgen05 kind::f16, BF16 in, FP32 in TMEM):
 //   S  = Q^_i K^T        (128 columns, lane = query row)
@@ -79,10 +83,9 @@ struct BwdBars {
   uint64_t buf_free;
   uint64_t dq_full;
   uint64_t drain;
-  uint64_t peer_free;   // rank 1: rank 0's shared memory may receive the partial dK/dV
-  uint64_t peer_data;   // rank 0: rank 1's partial dK/dV rows have landed
   uint32_t tmem_base;
   uint32_t abort_flag;
+  uint32_t split_order;  // split key tile: this CTA's position in the slot's count (0 or 1)
 };
 
 struct BwdArgs {
@@ -93,7 +96,9 @@ struct BwdArgs {
   int Sq, Sk;
   int n_qtiles, n_ktiles;
   int causal;
-  int split;  // 1: a cluster of 2 CTAs shares each key tile, each taking half its query tiles
+  int n_full;           // CTAs 0 .. n_full-1 own whole key tiles; then two CTAs per split tile
+  float* split_acc;     // [split tile][dK, dV][128 rows][D] FP32, zeroed by the preprocess
+  uint32_t* split_cnt;  // [split tile] CTAs done, zeroed by the preprocess
   float scale;
   float c2;   // scale * log2(e)
   uint32_t* err;
@@ -113,20 +118,21 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
 
   const int warp = warp_id();
   const int lane = lane_id();
-  // 1-D grid, key tiles fastest. With a split, CTAs 2p and 2p+1 form a cluster
-  // on key tile p: rank 0 takes the first half of its query tiles (rounded up),
-  // rank 1 the rest, and rank 0 stores the summed dK, dV.
+  // 1-D grid, key tiles fastest within a head. CTA n_full + 2 t + rank works
+  // on split key tile n_full + t: rank 0 takes the first half of its query
+  // tiles (rounded up), rank 1 the rest.
   const int lin = static_cast<int>(blockIdx.x);
-  const int rank = a.split ? (lin & 1) : 0;
-  const int pair = a.split ? (lin >> 1) : lin;
-  const int j = pair % a.n_ktiles;          // key tile
-  const int bh = pair / a.n_ktiles;
+  const bool split_cta = lin >= a.n_full;
+  const int sidx = split_cta ? (lin - a.n_full) >> 1 : 0;
+  const int rank = split_cta ? ((lin - a.n_full) & 1) : 0;
+  const int tile = split_cta ? a.n_full + sidx : lin;
+  const int j = tile % a.n_ktiles;          // key tile
+  const int bh = tile / a.n_ktiles;
   const int i_first = a.causal ? j : 0;     // BM == BN: the diagonal tile index equals j
   const int n_total = a.n_qtiles - i_first;
-  const int n_half0 = a.split ? (n_total + 1) / 2 : n_total;
+  const int n_half0 = split_cta ? (n_total + 1) / 2 : n_total;
   const int i_begin = rank == 0 ? i_first : i_first + n_half0;
   const int n_it = rank == 0 ? n_half0 : n_total - n_half0;
-  const int peer_n_it = a.split ? (rank == 0 ? n_total - n_half0 : n_half0) : 0;
 
   if (threadIdx.x == 0) {
     B.abort_flag = 0;
@@ -144,8 +150,6 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     mbar_init(&B.buf_free, 1);
     mbar_init(&B.dq_full, 1);
     mbar_init(&B.drain, 1);
-    mbar_init(&B.peer_free, 1);
-    mbar_init(&B.peer_data, 256);
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -154,7 +158,6 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (a.split) cluster_sync();   // the peer's barriers are initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem = B.tmem_base;
   const WaitCtl ctl{&B.abort_flag, a.err, a.timeout_ns};
@@ -339,49 +342,56 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       mbar_arrive(&B.ds_ready);
     }
     // Epilogue: warps 0-3 own dK rows (scaled), warps 4-7 dV rows, one key row
-    // per thread. With a split key tile, rank 1 writes its FP32 partial rows
-    // into rank 0's shared memory ([dK | dV][128 rows][D floats], 16-byte
-    // chunks swizzled by row) once rank 0's operands are no longer needed, and
-    // rank 0 stores the sums.
+    // per thread. A whole key tile stores BF16 rows. A split key tile adds its
+    // FP32 partial rows into the tile's workspace slot; after both CTAs have
+    // counted (device-scope fences around the count), the second one stores
+    // the BF16 sums. Neither waits for the other.
     const int krow = j * 128 + r;
     const uint32_t col = half == 0 ? L::kColDK : L::kColDV;
     const float mul = half == 0 ? a.scale : 1.0f;
-    const uint32_t prow = half * (128u * D * 4u) + r * (D * 4u);
-    if (ok && n_it > 0 && warp_wait(&B.buf_free, (n_it - 1) & 1, ctl)) {
-      tc_fence_after();
-      if (rank == 1) {
-        if (warp_wait_cluster(&B.peer_free, 0, ctl)) {
-          const uint32_t dst = mapa_shared(sbase + prow, 0);
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(tmem + lane_off + col + c * 32, v);
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-              st_cluster_v4(dst + (((c * 8 + q) ^ (r & 7)) << 4), v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-          }
-          mbar_arrive_remote(mapa_shared(smem_u32(&B.peer_data), 0));
-        }
-      } else {
-        // This CTA's MMAs are done: its operand tiles may be overwritten.
-        if (peer_n_it > 0 && warp == 0 && lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&B.peer_free), 1));
-        const bool add_peer = peer_n_it > 0 && warp_wait_cluster(&B.peer_data, 0, ctl);
-        bf16* out = (half == 0 ? a.dk : a.dv) + ((size_t)bh * a.Sk + krow) * D;
+    bf16* out = (half == 0 ? a.dk : a.dv) + ((size_t)bh * a.Sk + krow) * D;
+    const bool have = ok && n_it > 0 && warp_wait(&B.buf_free, (n_it - 1) & 1, ctl);
+    if (have) tc_fence_after();
+    if (!split_cta) {
+      if (have) {
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t v[32];
           tmem_ld32(tmem + lane_off + col + c * 32, v);
-          if (add_peer) {
+          if (krow < a.Sk) store_row32_bf16(out + c * 32, v, mul);
+        }
+      }
+    } else {
+      float* slot = a.split_acc + ((size_t)(sidx * 2 + half) * 128 + r) * D;
+      if (have) {
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_off + col + c * 32, v);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            red_add_v4(slot + c * 32 + 4 * q, __uint_as_float(v[4 * q]) * mul, __uint_as_float(v[4 * q + 1]) * mul,
+                       __uint_as_float(v[4 * q + 2]) * mul, __uint_as_float(v[4 * q + 3]) * mul);
+        }
+      }
+      __threadfence();
+      named_bar_sync(1, 256);                                  // all partial rows of this CTA are added
+      if (warp == 0 && lane == 0) B.split_order = atomicAdd(a.split_cnt + sidx, 1u);
+      named_bar_sync(1, 256);
+      if (B.split_order == 1u) {                                 // the other CTA's rows are in too
+        __threadfence();
+        if (krow < a.Sk) {
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t v[32];
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
-              const float4 pv = *reinterpret_cast<const float4*>(smem + prow + (((c * 8 + q) ^ (r & 7)) << 4));
-              v[4 * q] = __float_as_uint(__uint_as_float(v[4 * q]) + pv.x);
-              v[4 * q + 1] = __float_as_uint(__uint_as_float(v[4 * q + 1]) + pv.y);
-              v[4 * q + 2] = __float_as_uint(__uint_as_float(v[4 * q + 2]) + pv.z);
-              v[4 * q + 3] = __float_as_uint(__uint_as_float(v[4 * q + 3]) + pv.w);
+              const float4 t = __ldcg(reinterpret_cast<const float4*>(slot + c * 32 + 4 * q));
+              v[4 * q] = __float_as_uint(t.x), v[4 * q + 1] = __float_as_uint(t.y);
+              v[4 * q + 2] = __float_as_uint(t.z), v[4 * q + 3] = __float_as_uint(t.w);
             }
+            store_row32_bf16(out + c * 32, v, 1.0f);
           }
-          if (krow < a.Sk) store_row32_bf16(out + c * 32, v, mul);
         }
       }
     }
@@ -427,7 +437,6 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (a.split) cluster_sync();   // no CTA leaves while its peer may still reach its shared memory
   if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -437,8 +446,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
 }  // namespace
 
 cudaError_t launch_bwd(const Problem& p, const bf16* qh, const bf16* kh, const bf16* vh, const bf16* dout,
-                       const float* lse, const float* delta, float* dq_acc, bf16* dk, bf16* dv, uint32_t* err,
-                       cudaStream_t st) {
+                       const float* lse, const float* delta, float* dq_acc, bf16* dk, bf16* dv, float* split_acc,
+                       uint32_t* split_cnt, uint32_t* err, cudaStream_t st) {
   CUtensorMap tq, tk, tv, tdo, tdq;
   const uint64_t bh = p.bh();
   if (!make_tile_map(&tq, qh, false, p.D, p.Sq, bh, 64, 128) || !make_tile_map(&tk, kh, false, p.D, p.Sk, bh, 64, 128) ||
@@ -453,44 +462,54 @@ cudaError_t launch_bwd(const Problem& p, const bf16* qh, const bf16* kh, const b
   a.causal = p.causal ? 1 : 0;
   a.scale = p.scale, a.c2 = p.scale * kLog2e;
   a.err = err, a.timeout_ns = kWaitTimeoutNs;
-  // Split each key tile's query tiles between a cluster of 2 CTAs when even
-  // the split grid fits in one wave: then it halves the time of the only wave.
-  // With more key tiles the split's per-CTA costs (operand loads, pipeline
-  // fill and drain, the partial dK/dV exchange) outweigh the gain (measured on
-  // B=1 H=16 S=4096: 715 vs 779 TFLOP/s).
-  int sms = 0, dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    sms = 148;
-  const int64_t tiles = static_cast<int64_t>(a.n_ktiles) * static_cast<int64_t>(bh);
-  a.split = (2 * tiles <= static_cast<int64_t>(sms) && a.n_qtiles > 1) ? 1 : 0;
-  const int64_t blocks = tiles * (a.split ? 2 : 1);
-  if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
-
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
-  cfg.blockDim = dim3(kThreadsBwd, 1, 1);
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = a.split ? 2 : 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  const BwdSplit plan = bwd_split_plan(p, device_sm_count());
+  a.n_full = static_cast<int>(plan.n_full);
+  a.split_acc = split_acc, a.split_cnt = split_cnt;
+  const int64_t blocks = plan.n_full + 2 * plan.n_split;
+  if (blocks > 0x7fffffff || (plan.n_split > 0 && (split_acc == nullptr || split_cnt == nullptr)))
+    return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(blocks));
   if (p.D == 128) {
     cudaError_t e = set_smem(reinterpret_cast<const void*>(&bwd_kernel<128>), BwdLayout<128>::kAlloc);
     if (e != cudaSuccess) return e;
-    cfg.dynamicSmemBytes = BwdLayout<128>::kAlloc;
-    e = cudaLaunchKernelEx(&cfg, bwd_kernel<128>, tq, tk, tv, tdo, tdq, a);
-    if (e != cudaSuccess) return e;
+    bwd_kernel<128><<<grid, kThreadsBwd, BwdLayout<128>::kAlloc, st>>>(tq, tk, tv, tdo, tdq, a);
   } else {
     cudaError_t e = set_smem(reinterpret_cast<const void*>(&bwd_kernel<64>), BwdLayout<64>::kAlloc);
     if (e != cudaSuccess) return e;
-    cfg.dynamicSmemBytes = BwdLayout<64>::kAlloc;
-    e = cudaLaunchKernelEx(&cfg, bwd_kernel<64>, tq, tk, tv, tdo, tdq, a);
-    if (e != cudaSuccess) return e;
+    bwd_kernel<64><<<grid, kThreadsBwd, BwdLayout<64>::kAlloc, st>>>(tq, tk, tv, tdo, tdq, a);
   }
   return cudaGetLastError();
+}
+
+int device_sm_count() {
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return 148;
+  if (dev >= 0 && dev < 64) cache[dev] = sms;
+  return sms;
+}
+
+// Key tiles are uniform in a non-causal problem: with q full waves of
+// CTAs and r tiles left over, splitting those r tiles in two lets the last
+// wave run 2r half-length CTAs (when 2r <= SMs) instead of r full ones. A
+// problem whose every tile split fits one wave is split throughout.
+BwdSplit bwd_split_plan(const Problem& p, int sms) {
+  const int64_t nq = (p.Sq + kBlockM - 1) / kBlockM;
+  const int64_t tiles = ((p.Sk + kBlockN - 1) / kBlockN) * p.bh();
+  int64_t s = 0;
+  if (nq >= 2 && sms > 0) {
+    if (2 * tiles <= sms) {
+      s = tiles;
+    } else if (!p.causal) {
+      const int64_t r = tiles % sms;
+      s = 2 * r <= sms ? r : 0;
+    }
+  }
+  if (s > kMaxSplitTiles) s = 0;
+  return BwdSplit{tiles - s, s};
 }
 
 }  // namespace attnqat

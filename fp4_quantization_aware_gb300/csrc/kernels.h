@@ -26,10 +26,11 @@ cudaError_t launch_fake_bf16(const bf16* x, bf16* y, int64_t rows, int64_t cols,
 cudaError_t launch_fake_f32(const float* x, float* y, int64_t rows, int64_t cols, cudaStream_t st);
 
 // Q^, K^, V^ (and, when o_hp != nullptr, delta = rowsum(O' * dO) and a zeroed
-// FP32 dQ accumulator).
+// FP32 dQ accumulator); `zero_n` floats at `zero` are set to 0 as well (the
+// backward's split-tile counters and slots).
 cudaError_t launch_prep(const Problem& p, const bf16* q, const bf16* k, const bf16* v, const bf16* o_hp,
                         const bf16* dout, bf16* qh, bf16* kh, bf16* vh, float* delta, float* dq_acc,
-                        cudaStream_t st);
+                        float* zero, int64_t zero_n, cudaStream_t st);
 
 cudaError_t launch_nvfp4_pack(const bf16* x, uint8_t* packed, uint8_t* scales, int64_t rows, int64_t cols,
                               cudaStream_t st);
@@ -39,9 +40,24 @@ cudaError_t launch_dq_convert(const Problem& p, const float* dq_acc, bf16* dq, c
 cudaError_t launch_fwd(const Problem& p, const bf16* qh, const bf16* kh, const bf16* vh, bf16* o, bf16* o_hp,
                        float* lse, uint32_t* err, cudaStream_t st);
 
+// How the backward shares key tiles between CTAs: the first n_full key tiles
+// (in grid order) get one CTA each, the last n_split two CTAs each (half the
+// query tiles apiece), whose FP32 partial dK, dV meet in a workspace slot.
+constexpr int64_t kMaxSplitTiles = 96;
+struct BwdSplit {
+  int64_t n_full, n_split;
+};
+BwdSplit bwd_split_plan(const Problem& p, int sms);
+int device_sm_count();   // SMs of the current device (148 if it cannot be read)
+
+// Split-tile workspace: kMaxSplitTiles counters (rounded to 64 words), then
+// min(tiles, kMaxSplitTiles) slots of [dK, dV][128][D] FP32.
+inline int64_t split_cnt_words() { return 64 * ((kMaxSplitTiles + 63) / 64); }
+inline int64_t split_slot_floats(const Problem& p) { return 2 * 128 * p.D; }
+
 cudaError_t launch_bwd(const Problem& p, const bf16* qh, const bf16* kh, const bf16* vh, const bf16* dout,
-                       const float* lse, const float* delta, float* dq_acc, bf16* dk, bf16* dv, uint32_t* err,
-                       cudaStream_t st);
+                       const float* lse, const float* delta, float* dq_acc, bf16* dk, bf16* dv, float* split_acc,
+                       uint32_t* split_cnt, uint32_t* err, cudaStream_t st);
 
 // Inference forward: O = softmax(scale * Q K^T) V with packed NVFP4 Q and K
 // ((B*H, S, 64) bytes of E2M1 pairs, (B*H, S, 8) E4M3 scales) and BF16 V;

@@ -111,14 +111,25 @@ struct PrepArgs {
   const bf16* dout;
   float* delta;
   float* dq_acc;
+  float* zero;          // blockIdx.y == 3: zero_n16 runs of 16 floats set to 0
+  int64_t zero_n16;
 };
 
-// blockIdx.y selects the tensor (0: Q with delta, 1: K, 2: V).
+// blockIdx.y selects the tensor (0: Q with delta, 1: K, 2: V) or (3) the
+// range to zero.
 template <int D>
 __global__ void __launch_bounds__(kThreads) prep_kernel(PrepArgs a) {
   constexpr int kGroupsPerRow = D / 16;
   const int t = blockIdx.y;
   const int64_t g = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+  if (t == 3) {
+    if (g < a.zero_n16) {
+      float4* z = reinterpret_cast<float4*>(a.zero + g * 16);
+      const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[0] = zero, z[1] = zero, z[2] = zero, z[3] = zero;
+    }
+    return;
+  }
   const bool live = g < a.groups[t];
   if (blockIdx.x * static_cast<int64_t>(kThreads) >= a.groups[t]) return;   // whole block out of range
   float f[16];
@@ -224,15 +235,18 @@ cudaError_t launch_fake_f32(const float* x, float* y, int64_t rows, int64_t cols
 
 cudaError_t launch_prep(const Problem& p, const bf16* q, const bf16* k, const bf16* v, const bf16* o_hp,
                         const bf16* dout, bf16* qh, bf16* kh, bf16* vh, float* delta, float* dq_acc,
-                        cudaStream_t st) {
+                        float* zero, int64_t zero_n, cudaStream_t st) {
+  if (zero_n % 16 != 0) return cudaErrorInvalidValue;
   PrepArgs a;
   a.src[0] = q, a.src[1] = k, a.src[2] = v;
   a.dst[0] = qh, a.dst[1] = kh, a.dst[2] = vh;
   a.groups[0] = p.bh() * p.Sq * (p.D / 16);
   a.groups[1] = a.groups[2] = p.bh() * p.Sk * (p.D / 16);
   a.o_hp = o_hp, a.dout = dout, a.delta = delta, a.dq_acc = dq_acc;
-  const int64_t most = a.groups[0] > a.groups[1] ? a.groups[0] : a.groups[1];
-  dim3 grid(blocks_for(most), 3);
+  a.zero = zero, a.zero_n16 = zero == nullptr ? 0 : zero_n / 16;
+  int64_t most = a.groups[0] > a.groups[1] ? a.groups[0] : a.groups[1];
+  if (a.zero_n16 > most) most = a.zero_n16;
+  dim3 grid(blocks_for(most), a.zero_n16 > 0 ? 4 : 3);
   if (p.D == 128)
     prep_kernel<128><<<grid, kThreads, 0, st>>>(a);
   else

@@ -79,7 +79,9 @@ attnqat_status attnqat_check_support(const attnqat_problem* p);
 
 /* Workspace bytes for attnqat_fwd / attnqat_bwd (0 if the problem is not
  * supported). Forward: Q^, K^, V^ (BF16). Backward: Q^, K^, V^, delta (FP32,
- * B*H*Sq) and an FP32 dQ accumulator (B*H*Sq*D). */
+ * B*H*Sq), an FP32 dQ accumulator (B*H*Sq*D), and FP32 partial-dK/dV slots
+ * for up to 96 key tiles that the backward shares between two CTAs (the
+ * preprocess step zeroes what a call uses). */
 size_t attnqat_fwd_workspace_bytes(const attnqat_problem* p);
 size_t attnqat_bwd_workspace_bytes(const attnqat_problem* p);
 
@@ -121,14 +123,17 @@ attnqat_status attnqat_quantize_qkv(const attnqat_problem* p, const void* q, con
 attnqat_status attnqat_fwd_main(const attnqat_problem* p, void* o, void* o_hp, float* lse, void* workspace,
                                 size_t workspace_bytes, void* stream);
 
-/* Backward step 1: Q^, K^, V^, delta = rowsum(O' * dO) into the workspace and
- * the FP32 dQ accumulator zeroed (one HBM-bound kernel). */
+/* Backward step 1: Q^, K^, V^, delta = rowsum(O' * dO) into the workspace,
+ * the FP32 dQ accumulator and the split-tile slots zeroed (one HBM-bound
+ * kernel). */
 attnqat_status attnqat_bwd_preprocess(const attnqat_problem* p, const void* dout, const void* q, const void* k,
                                       const void* v, const void* o_hp, void* workspace, size_t workspace_bytes,
                                       void* stream);
 
-/* Backward step 2: the dK/dV kernel (one CTA per 128-key tile), which also
- * adds every tile's dQ contribution into the workspace's FP32 accumulator. */
+/* Backward step 2: the dK/dV kernel (one CTA per 128-key tile; when the
+ * tiles leave a partial last wave on the GPU, the last tiles get two CTAs
+ * each, half the query tiles apiece), which also adds every tile's dQ
+ * contribution into the workspace's FP32 accumulator. */
 attnqat_status attnqat_bwd_main(const attnqat_problem* p, const void* dout, const float* lse, void* dk, void* dv,
                                 void* workspace, size_t workspace_bytes, void* stream);
 

@@ -66,7 +66,15 @@ def test_workspace_sizes(clib):
     fwd = clib.attnqat_fwd_workspace_bytes(ctypes.byref(p))
     bwd = clib.attnqat_bwd_workspace_bytes(ctypes.byref(p))
     assert fwd == 3 * bh * 4096 * 128 * 2
-    assert bwd == fwd + bh * 4096 * 4 + bh * 4096 * 128 * 4
+    # + delta, the FP32 dQ accumulator, and the split-tile area: 128 counter
+    # words and FP32 [dK, dV] slots for min(key tiles, 96) tiles
+    split = 128 * 4 + min(bh * 4096 // 128, 96) * 2 * 128 * 128 * 4
+    assert bwd == fwd + bh * 4096 * 4 + bh * 4096 * 128 * 4 + split
+    small = attnqat.problem(1, 1, 100, 300, 64)      # 3 key tiles of 64-wide rows
+    assert clib.attnqat_bwd_workspace_bytes(ctypes.byref(small)) == (
+        256 * ((100 * 64 * 2 + 255) // 256) + 2 * 256 * ((300 * 64 * 2 + 255) // 256)
+        + 256 * ((100 * 4 + 255) // 256) + 256 * ((100 * 64 * 4 + 255) // 256)
+        + 256 * ((128 * 4 + 3 * 2 * 128 * 64 * 4 + 255) // 256))
     bad = attnqat.problem(1, 1, 10, 10, 96)
     assert clib.attnqat_fwd_workspace_bytes(ctypes.byref(bad)) == 0
 
