@@ -51,7 +51,7 @@ KERNEL_SOURCES = [os.path.join(ROOT, "fp4_quantization_aware_gb300", "csrc", f)
 METRIC = "QAT attn bwd TFLOP/s on 1 GB300 (fwd in fwd_tflops); % of dense BF16 peak in roofline"
 METRIC_INFER = "NVFP4 inference attn fwd TFLOP/s on 1 GB300 (pack Q/K + FP4 QK / BF16 PV kernel)"
 INFER_SOURCES = [os.path.join(ROOT, "fp4_quantization_aware_gb300", "csrc", f)
-                 for f in ("infer.cu", "attn_common.cuh", "nvfp4.cuh", "ptx.cuh")]
+                 for f in ("infer.cu", "fp4_mma.cuh", "attn_common.cuh", "nvfp4.cuh", "ptx.cuh")]
 PROFILE_INFER_JSON = os.path.join(ROOT, "profiles", "infer_kernel_ctx32k_counters.json")
 # exp2 results per clock per SM of the MUFU unit (ex2.approx), as measured on
 # this GPU by a throughput probe (16 lanes x 4 sub-partitions x 2 on the

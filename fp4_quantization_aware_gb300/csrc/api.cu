@@ -36,7 +36,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsLayout {
-  size_t qh, kh, vh, delta, dq_acc, split, split_slots, total;
+  size_t qh, kh, vh, delta, dq_acc, split, split_slots, q4, qsf, k4, ksf, total;
+  bool packed;   // forward with D = 128: NVFP4 Q, K for the first pass
 };
 
 Problem to_problem(const attnqat_problem& p) {
@@ -58,6 +59,12 @@ WsLayout layout(const attnqat_problem& p, bool bwd) {
     w.split_slots = static_cast<size_t>(tiles < kMaxSplitTiles ? tiles : kMaxSplitTiles);
     w.split = off,
     off += round256((split_cnt_words() + w.split_slots * split_slot_floats(to_problem(p))) * 4);
+  } else if (p.D == 128) {
+    w.packed = true;
+    w.q4 = off, off += round256(bh * p.Sq * 64);
+    w.qsf = off, off += round256(bh * p.Sq * 8);
+    w.k4 = off, off += round256(bh * p.Sk * 64);
+    w.ksf = off, off += round256(bh * p.Sk * 8);
   }
   w.total = off;
   return w;
@@ -241,7 +248,10 @@ attnqat_status attnqat_quantize_qkv(const attnqat_problem* p, const void* q, con
   ATTNQAT_TRY(check_ws(ws, ws_bytes, w.total));
   ATTNQAT_CUDA(launch_prep(to_problem(*p), static_cast<const bf16*>(q), static_cast<const bf16*>(k),
                            static_cast<const bf16*>(v), nullptr, nullptr, at<bf16>(ws, w.qh), at<bf16>(ws, w.kh),
-                           at<bf16>(ws, w.vh), nullptr, nullptr, nullptr, 0, static_cast<cudaStream_t>(stream)),
+                           at<bf16>(ws, w.vh), nullptr, nullptr, nullptr, 0,
+                           w.packed ? at<uint8_t>(ws, w.q4) : nullptr, w.packed ? at<uint8_t>(ws, w.qsf) : nullptr,
+                           w.packed ? at<uint8_t>(ws, w.k4) : nullptr, w.packed ? at<uint8_t>(ws, w.ksf) : nullptr,
+                           static_cast<cudaStream_t>(stream)),
                "quantize_qkv");
   return ATTNQAT_OK;
 }
@@ -256,6 +266,8 @@ attnqat_status attnqat_fwd_main(const attnqat_problem* p, void* o, void* o_hp, f
   uint32_t* err = device_error_word(&st);
   if (!err) return st;
   ATTNQAT_CUDA(launch_fwd(to_problem(*p), at<bf16>(ws, w.qh), at<bf16>(ws, w.kh), at<bf16>(ws, w.vh),
+                          w.packed ? at<uint8_t>(ws, w.q4) : nullptr, w.packed ? at<uint8_t>(ws, w.qsf) : nullptr,
+                          w.packed ? at<uint8_t>(ws, w.k4) : nullptr, w.packed ? at<uint8_t>(ws, w.ksf) : nullptr,
                           static_cast<bf16*>(o), static_cast<bf16*>(o_hp), lse, err, static_cast<cudaStream_t>(stream)),
                "fwd_main");
   return ATTNQAT_OK;
@@ -283,7 +295,7 @@ attnqat_status attnqat_bwd_preprocess(const attnqat_problem* p, const void* dout
                            at<float>(ws, w.split),
                            split_cnt_words() + bwd_split_plan(to_problem(*p), device_sm_count()).n_split *
                                                    split_slot_floats(to_problem(*p)),
-                           static_cast<cudaStream_t>(stream)),
+                           nullptr, nullptr, nullptr, nullptr, static_cast<cudaStream_t>(stream)),
                "bwd_preprocess");
   return ATTNQAT_OK;
 }

@@ -22,8 +22,17 @@
 // TMEM there. The next S goes into a buffer once the MMAs reading its P are
 // done. Warp roles (10 warps): 0-7 softmax (warp w: lanes 32*(w%4).., key
 // columns [64*(w/4), +64)); 8 TMA producer; 9 MMA issuer.
-// Shared memory (D = 128): Q^ 32K, K^ x2 64K, V^ x2 64K.
+// Shared memory (D = 128): Q^ 32K, K^ x2 64K, V^ x2 64K, NVFP4 Q 8K, NVFP4 K x2 16K.
+//
+// Pass 1 at D = 128 computes S on the block-scaled NVFP4 tensor-core MMA
+// (2 MMAs of K = 64 per tile instead of 8 BF16 ones) from the NVFP4 encoding
+// of Q and K, whose values are exactly Q^ and K^. Its scale factors sit in
+// the O' columns, which pass 1 does not use: Q scales at O' + [0,8), K scales
+// of tile t at O' + 16 + 16 (t % 2) + [0,8). The softmax warps write tile
+// t + 2's K scales once S(t) is complete, before releasing S(t); the first O'
+// MMA of pass 2 runs after every pass-1 MMA (issue order).
 #include "attn_common.cuh"
+#include "fp4_mma.cuh"
 
 namespace attnqat {
 namespace {
@@ -34,19 +43,27 @@ constexpr int kWarpMmaF = 9;
 
 template <int D>
 struct FwdLayout {
+  static constexpr bool kFp4 = D == 128;                 // pass 1 on the block-scaled NVFP4 MMA
   static constexpr uint32_t kTile = 128 * D * 2;
+  static constexpr uint32_t kFp4Tile = 128 * 64;         // 128 rows x 64 bytes of E2M1 pairs
   static constexpr uint32_t kQ = 0;
   static constexpr uint32_t kK0 = kQ + kTile;
   static constexpr uint32_t kK1 = kK0 + kTile;
   static constexpr uint32_t kV0 = kK1 + kTile;
   static constexpr uint32_t kV1 = kV0 + kTile;
-  static constexpr uint32_t kML = kV1 + kTile;           // 128 rows x (m, l) of half 1, then 128 lse2
+  static constexpr uint32_t kQ4 = kV1 + kTile;
+  static constexpr uint32_t kK40 = kQ4 + kFp4Tile;
+  static constexpr uint32_t kK41 = kK40 + kFp4Tile;
+  static constexpr uint32_t kML = kFp4 ? kK41 + kFp4Tile : kQ4;   // 128 rows x (m, l) of half 1, then 128 lse2
   static constexpr uint32_t kBar = kML + 1536;
   static constexpr uint32_t kBytes = kBar + 256;
   static constexpr uint32_t kAlloc = kBytes + 1024;
   static constexpr uint32_t kColS0 = 0;
   static constexpr uint32_t kColOP = 256;
   static constexpr uint32_t kColO = 256 + D;
+  static constexpr uint32_t kColSFQ = kColOP;            // pass 1 only
+  static constexpr uint32_t kColSFK0 = kColOP + 16;
+  static constexpr uint32_t kColSFK1 = kColOP + 32;
 };
 
 struct FwdBars {
@@ -62,11 +79,14 @@ struct FwdBars {
   uint64_t ml_ready;
   uint64_t lse_ready;
   uint64_t drain;
+  uint64_t sf_init;      // pass 1: Q scales and tile 0 and 1 K scales are in TMEM
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
 
 struct FwdArgs {
+  const uint8_t* q_sf;   // NVFP4 scales of Q, K ((B*H, S, D/16) E4M3), D = 128
+  const uint8_t* k_sf;
   bf16* o;
   bf16* o_hp;
   float* lse;
@@ -81,7 +101,8 @@ struct FwdArgs {
 template <int D>
 __global__ void __launch_bounds__(kThreadsFwd, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q4,
+               const __grid_constant__ CUtensorMap tm_k4, const FwdArgs a) {
   using L = FwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -111,6 +132,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     mbar_init(&B.ml_ready, 128);
     mbar_init(&B.lse_ready, 128);
     mbar_init(&B.drain, 1);
+    mbar_init(&B.sf_init, 256);
     fence_mbar_init();
   }
   if (warp == kWarpMmaF) {
@@ -127,17 +149,24 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q), tma_prefetch_desc(&tm_k), tma_prefetch_desc(&tm_v);
+      if (L::kFp4) tma_prefetch_desc(&tm_q4), tma_prefetch_desc(&tm_k4);
       int k_uses[2] = {0, 0}, v_uses[2] = {0, 0};
-      mbar_arrive_expect_tx(&B.q_full, L::kTile);
+      mbar_arrive_expect_tx(&B.q_full, L::kTile + (L::kFp4 ? L::kFp4Tile : 0));
       for (int b = 0; b < D / 64; ++b)
         tma_load_3d(smem + L::kQ + b * kBlockBytes, &tm_q, &B.q_full, b * 64, i * 128, bh);
+      if (L::kFp4) tma_load_3d(smem + L::kQ4, &tm_q4, &B.q_full, 0, i * 128, bh);
       for (int t = 0; t < nt; ++t) {
         const int jt = t < nk ? t : t - nk;
         const int s = t & 1;
         if (t >= 2 && !mbar_wait(&B.k_empty[s], ((t >> 1) - 1) & 1, ctl)) break;
-        mbar_arrive_expect_tx(&B.k_full[s], L::kTile);
-        for (int b = 0; b < D / 64; ++b)
-          tma_load_3d(smem + (s ? L::kK1 : L::kK0) + b * kBlockBytes, &tm_k, &B.k_full[s], b * 64, jt * 128, bh);
+        if (L::kFp4 && t < nk) {                          // pass 1: NVFP4 K
+          mbar_arrive_expect_tx(&B.k_full[s], L::kFp4Tile);
+          tma_load_3d(smem + (s ? L::kK41 : L::kK40), &tm_k4, &B.k_full[s], 0, jt * 128, bh);
+        } else {
+          mbar_arrive_expect_tx(&B.k_full[s], L::kTile);
+          for (int b = 0; b < D / 64; ++b)
+            tma_load_3d(smem + (s ? L::kK1 : L::kK0) + b * kBlockBytes, &tm_k, &B.k_full[s], b * 64, jt * 128, bh);
+        }
         ++k_uses[s];
         if (t >= nk) {
           const int tv = t - nk, sv = tv & 1;
@@ -176,11 +205,20 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         const int u = t - 2;
         if (u >= 0 && u < nk && !mbar_wait(&B.s_free[s], (u >> 1) & 1, ctl)) return false;
         tc_fence_after();
-        const uint64_t db = sdesc_advance(kmaj, s ? L::kK1 : L::kK0);
+        if (L::kFp4 && t < nk) {
+          const uint64_t d4q = sdesc_sw64(sbase + L::kQ4), d4k = sdesc_sw64(sbase + (s ? L::kK41 : L::kK40));
+          const uint32_t sfk = s ? L::kColSFK1 : L::kColSFK0;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t o = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
-          umma_bf16(tmem + L::kColS0 + s * 128, sdesc_advance(dq, o), sdesc_advance(db, o), kIdS, kk > 0);
+          for (int ks = 0; ks < 2; ++ks)
+            umma_nvfp4(tmem + L::kColS0 + s * 128, sdesc_advance(d4q, ks * 32), sdesc_advance(d4k, ks * 32),
+                       idesc_nvfp4(128, 128), tmem + L::kColSFQ + ks * 4, tmem + sfk + ks * 4, ks > 0);
+        } else {
+          const uint64_t db = sdesc_advance(kmaj, s ? L::kK1 : L::kK0);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t o = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
+            umma_bf16(tmem + L::kColS0 + s * 128, sdesc_advance(dq, o), sdesc_advance(db, o), kIdS, kk > 0);
+          }
         }
         umma_commit(&B.s_full[s]);
         umma_commit(&B.k_empty[s]);
@@ -197,7 +235,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
           umma_bf16_tmem_a(tmem + col, tmem + ac, sdesc_advance(dv, kk * 2048), kIdO, (acc || kk > 0) ? 1u : 0u);
         }
       };
-      bool ok = mbar_wait(&B.q_full, 0, ctl) && issue_s(0);
+      bool ok = mbar_wait(&B.q_full, 0, ctl) && (!L::kFp4 || mbar_wait(&B.sf_init, 0, ctl)) && issue_s(0);
       for (int t = 0; ok && t < nt; ++t) {
         if (t + 1 < nt && !issue_s(t + 1)) break;
         if (t >= nk) {
@@ -226,13 +264,30 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     const uint32_t lane_off = (quarter * 32u) << 16;
     const int qrow = i * 128 + r;
     const int kend = a.causal ? min(a.Sk, qrow + 1) : a.Sk;
+    const int64_t kbase = static_cast<int64_t>(bh) * a.Sk;
     bool ok = true;
+    if (L::kFp4) {   // pass-1 scale factors: this warp writes K step `half` of each block
+      uint32_t w[4];
+      load_scales(a.q_sf, static_cast<int64_t>(bh) * a.Sq + i * 128, min(128, a.Sq - i * 128), half, w);
+      tmem_st4(tmem + lane_off + L::kColSFQ + 4 * half, w);
+      load_scales(a.k_sf, kbase, min(128, a.Sk), half, w);
+      tmem_st4(tmem + lane_off + L::kColSFK0 + 4 * half, w);
+      if (nk > 1) {
+        load_scales(a.k_sf, kbase + 128, min(128, a.Sk - 128), half, w);
+        tmem_st4(tmem + lane_off + L::kColSFK1 + 4 * half, w);
+      }
+      tc_fence_before();
+      mbar_arrive(&B.sf_init);
+    }
 
     // pass 1: running max and sum of exp2(S * c2) over this thread's key columns
     float m = -INFINITY, l = 0.0f;
     for (int t = 0; t < nk; ++t) {
       const int s = t & 1;
       const int valid = kend - (t * 128 + static_cast<int>(half) * 64);
+      const bool more = L::kFp4 && t + 2 < nk;
+      uint32_t sfw[4] = {0u, 0u, 0u, 0u};
+      if (more) load_scales(a.k_sf, kbase + (t + 2) * 128, min(128, a.Sk - (t + 2) * 128), half, sfw);
       if (!warp_wait(&B.s_full[s], (t >> 1) & 1, ctl)) { ok = false; break; }
       tc_fence_after();
       float x[64];
@@ -242,6 +297,9 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
 #pragma unroll
         for (int k = 0; k < 64; ++k) x[k] = (k < valid) ? __uint_as_float(v[k]) * a.c2 : -INFINITY;
       }
+      // tile t + 2's K scales into the buffer S(t) used (S(t) is complete);
+      // releasing S(t) below also certifies them to the MMA issuer
+      if (more) tmem_st4(tmem + lane_off + (s ? L::kColSFK1 : L::kColSFK0) + 4 * half, sfw);
       tc_fence_before();
       mbar_arrive(&B.s_free[s]);
       // four independent chains for the row max and the row sum (ILP)
@@ -341,14 +399,23 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
 
 }  // namespace
 
-cudaError_t launch_fwd(const Problem& p, const bf16* qh, const bf16* kh, const bf16* vh, bf16* o, bf16* o_hp,
-                       float* lse, uint32_t* err, cudaStream_t st) {
-  CUtensorMap tq, tk, tv;
+cudaError_t launch_fwd(const Problem& p, const bf16* qh, const bf16* kh, const bf16* vh, const uint8_t* q4,
+                       const uint8_t* qsf, const uint8_t* k4, const uint8_t* ksf, bf16* o, bf16* o_hp, float* lse,
+                       uint32_t* err, cudaStream_t st) {
+  CUtensorMap tq, tk, tv, tq4, tk4;
   const uint64_t bh = p.bh();
   if (!make_tile_map(&tq, qh, false, p.D, p.Sq, bh, 64, 128) || !make_tile_map(&tk, kh, false, p.D, p.Sk, bh, 64, 128) ||
       !make_tile_map(&tv, vh, false, p.D, p.Sk, bh, 64, 128))
     return cudaErrorInvalidValue;
+  const bool fp4 = p.D == 128;
+  if (fp4 && (q4 == nullptr || qsf == nullptr || k4 == nullptr || ksf == nullptr)) return cudaErrorInvalidValue;
+  if (fp4) {
+    if (!make_fp4_map(&tq4, q4, p.Sq, bh, 128) || !make_fp4_map(&tk4, k4, p.Sk, bh, 128)) return cudaErrorInvalidValue;
+  } else {
+    tq4 = tq, tk4 = tk;   // not read at D = 64
+  }
   FwdArgs a;
+  a.q_sf = qsf, a.k_sf = ksf;
   a.o = o, a.o_hp = o_hp, a.lse = lse;
   a.Sq = static_cast<int>(p.Sq), a.Sk = static_cast<int>(p.Sk);
   a.n_qtiles = static_cast<int>((p.Sq + kBlockM - 1) / kBlockM);
@@ -357,14 +424,14 @@ cudaError_t launch_fwd(const Problem& p, const bf16* qh, const bf16* kh, const b
   a.c2 = p.scale * kLog2e;
   a.err = err, a.timeout_ns = kWaitTimeoutNs;
   const dim3 grid(static_cast<unsigned>(a.n_qtiles), static_cast<unsigned>(bh));
-  if (p.D == 128) {
+  if (fp4) {
     cudaError_t e = set_smem(reinterpret_cast<const void*>(&fwd_kernel<128>), FwdLayout<128>::kAlloc);
     if (e != cudaSuccess) return e;
-    fwd_kernel<128><<<grid, kThreadsFwd, FwdLayout<128>::kAlloc, st>>>(tq, tk, tv, a);
+    fwd_kernel<128><<<grid, kThreadsFwd, FwdLayout<128>::kAlloc, st>>>(tq, tk, tv, tq4, tk4, a);
   } else {
     cudaError_t e = set_smem(reinterpret_cast<const void*>(&fwd_kernel<64>), FwdLayout<64>::kAlloc);
     if (e != cudaSuccess) return e;
-    fwd_kernel<64><<<grid, kThreadsFwd, FwdLayout<64>::kAlloc, st>>>(tq, tk, tv, a);
+    fwd_kernel<64><<<grid, kThreadsFwd, FwdLayout<64>::kAlloc, st>>>(tq, tk, tv, tq4, tk4, a);
   }
   return cudaGetLastError();
 }

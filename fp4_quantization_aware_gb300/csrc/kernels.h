@@ -27,18 +27,24 @@ cudaError_t launch_fake_f32(const float* x, float* y, int64_t rows, int64_t cols
 
 // Q^, K^, V^ (and, when o_hp != nullptr, delta = rowsum(O' * dO) and a zeroed
 // FP32 dQ accumulator); `zero_n` floats at `zero` are set to 0 as well (the
-// backward's split-tile counters and slots).
+// backward's split-tile counters and slots). When q4 / k4 are not null, Q and
+// K are also written NVFP4-encoded ((rows, D/2) bytes of E2M1 pairs and
+// (rows, D/16) E4M3 scales): the forward's first pass reads them.
 cudaError_t launch_prep(const Problem& p, const bf16* q, const bf16* k, const bf16* v, const bf16* o_hp,
                         const bf16* dout, bf16* qh, bf16* kh, bf16* vh, float* delta, float* dq_acc,
-                        float* zero, int64_t zero_n, cudaStream_t st);
+                        float* zero, int64_t zero_n, uint8_t* q4, uint8_t* qsf, uint8_t* k4, uint8_t* ksf,
+                        cudaStream_t st);
 
 cudaError_t launch_nvfp4_pack(const bf16* x, uint8_t* packed, uint8_t* scales, int64_t rows, int64_t cols,
                               cudaStream_t st);
 
 cudaError_t launch_dq_convert(const Problem& p, const float* dq_acc, bf16* dq, cudaStream_t st);
 
-cudaError_t launch_fwd(const Problem& p, const bf16* qh, const bf16* kh, const bf16* vh, bf16* o, bf16* o_hp,
-                       float* lse, uint32_t* err, cudaStream_t st);
+// The forward; q4, qsf, k4, ksf: NVFP4 Q and K for the first pass's
+// block-scaled S (D = 128; null for D = 64, which stays on BF16).
+cudaError_t launch_fwd(const Problem& p, const bf16* qh, const bf16* kh, const bf16* vh, const uint8_t* q4,
+                       const uint8_t* qsf, const uint8_t* k4, const uint8_t* ksf, bf16* o, bf16* o_hp, float* lse,
+                       uint32_t* err, cudaStream_t st);
 
 // How the backward shares key tiles between CTAs: the first n_full key tiles
 // (in grid order) get one CTA each, the last n_split two CTAs each (half the

@@ -113,6 +113,8 @@ struct PrepArgs {
   float* dq_acc;
   float* zero;          // blockIdx.y == 3: zero_n16 runs of 16 floats set to 0
   int64_t zero_n16;
+  uint8_t* packed[2];   // Q, K as NVFP4 (E2M1 pairs), or null
+  uint8_t* scales[2];   // their E4M3 group scales
 };
 
 // blockIdx.y selects the tensor (0: Q with delta, 1: K, 2: V) or (3) the
@@ -135,6 +137,14 @@ __global__ void __launch_bounds__(kThreads) prep_kernel(PrepArgs a) {
   float f[16];
   if (live) {
     load16(a.src[t] + g * 16, f);
+    if (t < 2 && a.packed[t] != nullptr) {   // the same values, NVFP4-encoded
+      uint8_t b[8];
+      a.scales[t][g] = nvfp4_encode_16(f, b);
+      uint2 w;
+      w.x = b[0] | (uint32_t)b[1] << 8 | (uint32_t)b[2] << 16 | (uint32_t)b[3] << 24;
+      w.y = b[4] | (uint32_t)b[5] << 8 | (uint32_t)b[6] << 16 | (uint32_t)b[7] << 24;
+      reinterpret_cast<uint2*>(a.packed[t])[g] = w;
+    }
     fake_nvfp4_16(f);
     store16(a.dst[t] + g * 16, f);
   }
@@ -235,9 +245,11 @@ cudaError_t launch_fake_f32(const float* x, float* y, int64_t rows, int64_t cols
 
 cudaError_t launch_prep(const Problem& p, const bf16* q, const bf16* k, const bf16* v, const bf16* o_hp,
                         const bf16* dout, bf16* qh, bf16* kh, bf16* vh, float* delta, float* dq_acc,
-                        float* zero, int64_t zero_n, cudaStream_t st) {
+                        float* zero, int64_t zero_n, uint8_t* q4, uint8_t* qsf, uint8_t* k4, uint8_t* ksf,
+                        cudaStream_t st) {
   if (zero_n % 16 != 0) return cudaErrorInvalidValue;
   PrepArgs a;
+  a.packed[0] = q4, a.scales[0] = qsf, a.packed[1] = k4, a.scales[1] = ksf;
   a.src[0] = q, a.src[1] = k, a.src[2] = v;
   a.dst[0] = qh, a.dst[1] = kh, a.dst[2] = vh;
   a.groups[0] = p.bh() * p.Sq * (p.D / 16);

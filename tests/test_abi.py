@@ -65,11 +65,13 @@ def test_workspace_sizes(clib):
     bh = 16
     fwd = clib.attnqat_fwd_workspace_bytes(ctypes.byref(p))
     bwd = clib.attnqat_bwd_workspace_bytes(ctypes.byref(p))
-    assert fwd == 3 * bh * 4096 * 128 * 2
+    # Q^, K^, V^ (BF16) and, at D = 128, NVFP4 Q and K (E2M1 pairs + E4M3 scales)
+    assert fwd == 3 * bh * 4096 * 128 * 2 + 2 * (bh * 4096 * 64 + bh * 4096 * 8)
+    base = 3 * bh * 4096 * 128 * 2
     # + delta, the FP32 dQ accumulator, and the split-tile area: 128 counter
     # words and FP32 [dK, dV] slots for min(key tiles, 96) tiles
     split = 128 * 4 + min(bh * 4096 // 128, 96) * 2 * 128 * 128 * 4
-    assert bwd == fwd + bh * 4096 * 4 + bh * 4096 * 128 * 4 + split
+    assert bwd == base + bh * 4096 * 4 + bh * 4096 * 128 * 4 + split
     small = attnqat.problem(1, 1, 100, 300, 64)      # 3 key tiles of 64-wide rows
     assert clib.attnqat_bwd_workspace_bytes(ctypes.byref(small)) == (
         256 * ((100 * 64 * 2 + 255) // 256) + 2 * 256 * ((300 * 64 * 2 + 255) // 256)
