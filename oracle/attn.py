@@ -220,6 +220,69 @@ def infer_fwd(q, k, v, scale, causal=False, quantize=True):
     return o, lse
 
 
+R2_BLOCK_N = 128
+
+
+def r2_rows(qh, kh, vh, scale, causal, r0, r1, block_n=R2_BLOCK_N, quantize=True):
+    """Recipe R2, the one-pass forward, for query rows [r0, r1) of one head:
+    (O, O', LSE).
+
+    This is the variant that the review of the FastVideo pull request "Add
+    Attn-QAT training Triton kernels" points at (its FP8-P branch sums the row
+    statistic from the unquantized probabilities). Each query row takes the
+    key tiles of ``block_n`` keys in order, with an online softmax:
+
+        m_j   = max(m_{j-1}, max_k S_jk)          the exact running max
+        P_j   = exp(S_j - m_j)                    unnormalised
+        P^_j  = fake_nvfp4(fl32(P_j))             groups of 16 keys of the tile
+        a_j   = exp(m_{j-1} - m_j)
+        l_j   = a_j l_{j-1} + rowsum(P_j)         from the unquantized P
+        O'_j  = a_j O'_{j-1} + P_j V^_j
+        O_j   = a_j O_{j-1} + P^_j V^_j
+
+    with O = O_n / l_n, O' = O'_n / l_n and LSE = m_n + ln l_n. O' and LSE
+    equal the standard forward's, so the backward is the same; only O
+    differs, because P^ is formed before normalisation."""
+    s = _logits(qh[r0:r1], kh, scale, causal, r0)
+    n, Sk = s.shape[0], s.shape[1]
+    m = np.full(n, -np.inf)
+    l = np.zeros(n)
+    acc = np.zeros((n, vh.shape[1]))
+    acc_hp = np.zeros((n, vh.shape[1]))
+    for c0 in range(0, Sk, block_n):
+        c1 = min(Sk, c0 + block_n)
+        st = s[:, c0:c1]
+        m_new = np.maximum(m, np.max(st, axis=1))
+        live = np.isfinite(m_new)                      # rows with a key so far
+        a = np.where(np.isfinite(m), np.exp(m - np.where(live, m_new, 0.0)), 0.0)
+        p = np.where(live[:, None], np.exp(st - np.where(live, m_new, 0.0)[:, None]), 0.0)
+        l = a * l + p.sum(axis=1)
+        acc = a[:, None] * acc + p_hat(p, quantize) @ vh[c0:c1]
+        acc_hp = a[:, None] * acc_hp + p @ vh[c0:c1]
+        m = m_new
+    return acc / l[:, None], acc_hp / l[:, None], m + np.log(l)
+
+
+def r2_fwd(q, k, v, scale, causal=False, block_n=R2_BLOCK_N, quantize=True):
+    """Recipe R2 on BHSD float64 arrays: (O, O', LSE) (see r2_rows); Q^, K^,
+    V^ are fake_nvfp4 of Q, K, V as in the standard forward."""
+    q, k, v = (np.asarray(t, np.float64) for t in (q, k, v))
+    if causal and q.shape[2] != k.shape[2]:
+        raise ValueError("causal attention needs Sq == Sk")
+    qh, kh, vh = hats(q, k, v, quantize)
+    B, H, Sq, _ = q.shape
+    o = np.empty((B, H, Sq, v.shape[3]))
+    o_hp = np.empty_like(o)
+    lse = np.empty((B, H, Sq))
+    for b in range(B):
+        for h in range(H):
+            for r0 in range(0, Sq, ROW_BLOCK):
+                r1 = min(Sq, r0 + ROW_BLOCK)
+                o[b, h, r0:r1], o_hp[b, h, r0:r1], lse[b, h, r0:r1] = r2_rows(
+                    qh[b, h], kh[b, h], vh[b, h], scale, causal, r0, r1, block_n, quantize)
+    return o, o_hp, lse
+
+
 def nvfp4_codes(x, axis=-1):
     """NVFP4 encoding of x along ``axis``: (E2M1 codes, E4M3 scale codes).
 

@@ -17,6 +17,7 @@ Each check uses something other than the oracle's own formulas:
   an enumeration quantizer.
 """
 import math
+import os
 
 import numpy as np
 import pytest
@@ -233,3 +234,106 @@ def test_nvfp4_codes_decode_to_fake_quantized_values():
     mag = E2[codes & 7] * np.repeat(E4[sc], 16, axis=1)
     dec = np.where(codes & 8, -mag, mag)
     np.testing.assert_array_equal(dec.view(np.int64), nvfp4.fake_nvfp4(x).view(np.int64))
+
+
+# ------------------------------------------------------------------ recipe R2
+def _golden_rows(name):
+    import math
+    path = os.path.join(os.path.dirname(__file__), "golden", name)
+    rows = []
+    for line in open(path):
+        if not line.strip() or line.startswith("#"):
+            continue
+        tag, bn, logits, c_r2, c_std = (f.strip() for f in line.split("|"))
+
+        def vals(txt):
+            out = []
+            for tok in txt.split(","):
+                tok = tok.strip()
+                rep = 1
+                if "*" in tok:
+                    tok, rep = tok.split("*")
+                    rep = int(rep)
+                out += [float(eval(tok, {"__builtins__": {}}, {"ln2": math.log(2.0)}))] * rep
+            return np.array(out)
+        rows.append((tag, int(bn), vals(logits), vals(c_r2), vals(c_std)))
+    return rows
+
+
+@pytest.mark.parametrize("case", _golden_rows("r2_worked.txt"), ids=lambda c: c[0])
+def test_r2_worked_examples(case):
+    """Hand-derived R2 outputs (tests/golden/r2_worked.txt): one query row whose
+    logits are given directly (Q^ = e_0, K^_j = S_j e_0, scale 1), V^ = identity."""
+    _, bn, logits, c_r2, c_std = case
+    Sk = len(logits)
+    qh = np.zeros((1, 16)); qh[0, 0] = 1.0
+    kh = np.zeros((Sk, 16)); kh[:, 0] = logits
+    vh = np.eye(Sk)
+    o, o_hp, lse = attn.r2_rows(qh, kh, vh, 1.0, False, 0, 1, block_n=bn)
+    np.testing.assert_allclose(o[0], c_r2, rtol=1e-12, atol=1e-12)
+    o_std, _, _ = attn.fwd_rows(qh, kh, vh, 1.0, False, 0, 1)
+    np.testing.assert_allclose(o_std[0], c_std, rtol=1e-12, atol=1e-12)
+    p = np.exp(logits - logits.max())
+    np.testing.assert_allclose(o_hp[0], p / p.sum(), rtol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_r2_identity_matches_sdpa(causal):
+    q, k, v, _ = _inputs(1, 2, 45, 45, 16, 31)
+    o, o_hp, lse = attn.r2_fwd(q, k, v, 0.3, causal, block_n=16, quantize=False)
+    ref = torch.nn.functional.scaled_dot_product_attention(torch.tensor(q), torch.tensor(k), torch.tensor(v),
+                                                           is_causal=causal, scale=0.3).numpy()
+    np.testing.assert_allclose(o, ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(o_hp, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_r2_auxiliary_outputs_are_the_standard_ones():
+    """The online rescaling leaves O' = P V^ and the LSE exactly those of the
+    standard forward (the backward's inputs), whatever the tile size."""
+    q, k, v, _ = _inputs(1, 2, 70, 70, 32, 32, gain=2.0)
+    o_s, ohp_s, lse_s = attn.attn_qat_fwd(q, k, v, 0.2, True)
+    for bn in (16, 32, 128):
+        o, o_hp, lse = attn.r2_fwd(q, k, v, 0.2, True, block_n=bn)
+        np.testing.assert_allclose(o_hp, ohp_s, rtol=1e-11, atol=1e-13)
+        np.testing.assert_allclose(lse, lse_s, rtol=1e-13)
+        assert np.linalg.norm(o - o_s) > 1e-3 * np.linalg.norm(o_s)   # O is a different recipe
+
+
+def _brute_r2(q, k, v, scale, causal, bn):
+    """Scalar pure-Python recipe R2 on one head with the enumeration quantizer."""
+    Sq, D, Sk = len(q), len(q[0]), len(k)
+    quant = lambda row: sum((list(brute_group(row[g:g + 16])) for g in range(0, len(row), 16)), [])
+    qh, kh, vh = [quant(r) for r in q], [quant(r) for r in k], [quant(r) for r in v]
+    O, Ohp, L = [], [], []
+    for i in range(Sq):
+        m, l = -math.inf, 0.0
+        acc, acc_hp = [0.0] * D, [0.0] * D
+        for c0 in range(0, Sk, bn):
+            keys = range(c0, min(Sk, c0 + bn))
+            s = [scale * sum(qh[i][d] * kh[j][d] for d in range(D)) if not (causal and j > i) else -math.inf
+                 for j in keys]
+            m_new = max([m] + s)
+            a = math.exp(m - m_new) if m > -math.inf else 0.0
+            p = [math.exp(x - m_new) if x > -math.inf else 0.0 for x in s]
+            p32 = [float(np.float32(x)) for x in p]
+            ph = []
+            for g in range(0, len(p32), 16):
+                seg = p32[g:g + 16]
+                ph += list(brute_group(seg + [0.0] * (16 - len(seg))))[:len(seg)]
+            l = a * l + sum(p)
+            acc = [a * acc[d] + sum(ph[t] * vh[j][d] for t, j in enumerate(keys)) for d in range(D)]
+            acc_hp = [a * acc_hp[d] + sum(p[t] * vh[j][d] for t, j in enumerate(keys)) for d in range(D)]
+            m = m_new
+        O.append([x / l for x in acc]), Ohp.append([x / l for x in acc_hp]), L.append(m + math.log(l))
+    return np.array(O), np.array(Ohp), np.array(L)
+
+
+@pytest.mark.parametrize("Sq,causal", [(6, False), (40, True)])
+def test_r2_matches_brute_force(Sq, causal):
+    """Three key tiles of 16 (the last ragged), causal diagonals included."""
+    q, k, v, _ = _inputs(1, 1, Sq, 40, 16, 33, gain=3.0)
+    bo, bohp, bl = _brute_r2(q[0, 0].tolist(), k[0, 0].tolist(), v[0, 0].tolist(), 0.25, causal, 16)
+    o, o_hp, lse = attn.r2_fwd(q, k, v, 0.25, causal, block_n=16)
+    np.testing.assert_allclose(o[0, 0], bo, rtol=1e-9, atol=1e-12)
+    np.testing.assert_allclose(o_hp[0, 0], bohp, rtol=1e-9, atol=1e-12)
+    np.testing.assert_allclose(lse[0, 0], bl, rtol=1e-12)
