@@ -61,6 +61,8 @@ SIGNATURES = {
     "attnqat_infer_fwd_workspace_bytes": (ctypes.c_size_t, [_PP]),
     "attnqat_infer_fwd_packed": (_S, [_PP, _P, _P, _P, _P, _P, _P, _P, _P]),
     "attnqat_infer_fwd": (_S, [_PP, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "attnqat_fwd_r2": (_S, [_PP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "attnqat_fwd_main_r2": (_S, [_PP, _P, _P, _P, _P, ctypes.c_size_t, _P]),
 }
 
 _lib = None
@@ -155,6 +157,29 @@ def fwd(q, k, v, causal=False, scale=None, ws=None, out=None, stream=None):
         o, o_hp, lse = out
     check(lib.attnqat_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(o_hp), _ptr(lse), _ptr(ws),
                           ws.numel(), _stream(stream)), "attnqat_fwd")
+    return o, o_hp, lse
+
+
+def fwd_r2(q, k, v, causal=False, scale=None, ws=None, out=None, stream=None):
+    """Forward in recipe R2 (each key tile's P quantized before normalisation):
+    returns (O, O', LSE) for BHSD BF16 CUDA tensors; O' and LSE are those of
+    ``fwd``, so ``bwd`` applies unchanged."""
+    import torch
+    _bf16_contig(q, k, v)
+    p = _problem_of(q, k, causal, scale)
+    lib = load()
+    need = lib.attnqat_fwd_workspace_bytes(ctypes.byref(p))
+    if need == 0:
+        check(lib.attnqat_check_support(ctypes.byref(p)), "attnqat_check_support")
+    if ws is None:
+        ws = workspace(need, q.device)
+    if out is None:
+        o, o_hp = torch.empty_like(q), torch.empty_like(q)
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    else:
+        o, o_hp, lse = out
+    check(lib.attnqat_fwd_r2(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(o_hp), _ptr(lse), _ptr(ws),
+                             ws.numel(), _stream(stream)), "attnqat_fwd_r2")
     return o, o_hp, lse
 
 

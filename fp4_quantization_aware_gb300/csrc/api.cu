@@ -282,6 +282,31 @@ attnqat_status attnqat_fwd(const attnqat_problem* p, const void* q, const void* 
   return attnqat_fwd_main(p, o, o_hp, lse, ws, ws_bytes, stream);
 }
 
+attnqat_status attnqat_fwd_main_r2(const attnqat_problem* p, void* o, void* o_hp, float* lse, void* ws,
+                                   size_t ws_bytes, void* stream) {
+  ATTNQAT_TRY(check_problem(p));
+  ATTNQAT_TRY(check_ptrs({o, o_hp, lse}));
+  const WsLayout w = layout(*p, false);
+  ATTNQAT_TRY(check_ws(ws, ws_bytes, w.total));
+  attnqat_status st = ATTNQAT_OK;
+  uint32_t* err = device_error_word(&st);
+  if (!err) return st;
+  ATTNQAT_CUDA(launch_fwd_r2(to_problem(*p), at<bf16>(ws, w.qh), at<bf16>(ws, w.kh), at<bf16>(ws, w.vh),
+                             static_cast<bf16*>(o), static_cast<bf16*>(o_hp), lse, err,
+                             static_cast<cudaStream_t>(stream)),
+               "fwd_main_r2");
+  return ATTNQAT_OK;
+}
+
+attnqat_status attnqat_fwd_r2(const attnqat_problem* p, const void* q, const void* k, const void* v, void* o,
+                              void* o_hp, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  ATTNQAT_TRY(check_problem(p));
+  ATTNQAT_TRY(check_ptrs({q, k, v, o, o_hp, lse}));
+  ATTNQAT_TRY(check_ws(ws, ws_bytes, layout(*p, false).total));
+  ATTNQAT_TRY(attnqat_quantize_qkv(p, q, k, v, ws, ws_bytes, stream));
+  return attnqat_fwd_main_r2(p, o, o_hp, lse, ws, ws_bytes, stream);
+}
+
 attnqat_status attnqat_bwd_preprocess(const attnqat_problem* p, const void* dout, const void* q, const void* k,
                                       const void* v, const void* o_hp, void* ws, size_t ws_bytes, void* stream) {
   ATTNQAT_TRY(check_problem(p));

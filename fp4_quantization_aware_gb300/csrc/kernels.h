@@ -61,6 +61,11 @@ int device_sm_count();   // SMs of the current device (148 if it cannot be read)
 inline int64_t split_cnt_words() { return 64 * ((kMaxSplitTiles + 63) / 64); }
 inline int64_t split_slot_floats(const Problem& p) { return 2 * 128 * p.D; }
 
+// The forward in recipe R2 (one pass; P^ of each key tile quantized before
+// normalisation) from the quantize step's Q^, K^, V^; same outputs as launch_fwd.
+cudaError_t launch_fwd_r2(const Problem& p, const bf16* qh, const bf16* kh, const bf16* vh, bf16* o, bf16* o_hp,
+                          float* lse, uint32_t* err, cudaStream_t st);
+
 cudaError_t launch_bwd(const Problem& p, const bf16* qh, const bf16* kh, const bf16* vh, const bf16* dout,
                        const float* lse, const float* delta, float* dq_acc, bf16* dk, bf16* dv, float* split_acc,
                        uint32_t* split_cnt, uint32_t* err, cudaStream_t st);

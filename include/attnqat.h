@@ -123,6 +123,24 @@ attnqat_status attnqat_quantize_qkv(const attnqat_problem* p, const void* q, con
 attnqat_status attnqat_fwd_main(const attnqat_problem* p, void* o, void* o_hp, float* lse, void* workspace,
                                 size_t workspace_bytes, void* stream);
 
+/* ---- forward recipe R2 ---- */
+
+/* The forward in recipe R2: one pass over the key tiles with an online
+ * softmax that fake-quantizes each 128-key tile's unnormalised probabilities
+ * (the FastVideo pull request "Add Attn-QAT training Triton kernels", review
+ * of its FP8-P branch: the row statistic is summed from the unquantized P).
+ * Per query row and key tile j: m_j = running max of the scaled logits,
+ * P^_j = fake_nvfp4(exp(S_j - m_j)) in groups of 16 keys, and
+ * O = sum_j exp(m_j - m) P^_j V^_j / l. O' = P V^ and the natural-log LSE are
+ * the standard forward's (so attnqat_bwd applies unchanged); only O differs.
+ * Same arguments, workspace and outputs as attnqat_fwd. */
+attnqat_status attnqat_fwd_r2(const attnqat_problem* p, const void* q, const void* k, const void* v, void* o,
+                              void* o_hp, float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Step 2 of attnqat_fwd_r2, after attnqat_quantize_qkv. */
+attnqat_status attnqat_fwd_main_r2(const attnqat_problem* p, void* o, void* o_hp, float* lse, void* workspace,
+                                   size_t workspace_bytes, void* stream);
+
 /* Backward step 1: Q^, K^, V^, delta = rowsum(O' * dO) into the workspace,
  * the FP32 dQ accumulator and the split-tile slots zeroed (one HBM-bound
  * kernel). */
