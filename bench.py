@@ -173,9 +173,11 @@ def run_ours(args, w, rank, world, local_rank):
     sp = stream.cuda_stream
     P = lambda a: a.data_ptr()  # noqa: E731
 
+    fwd_main = lib.attnqat_fwd_main_r2 if args.recipe == "r2" else lib.attnqat_fwd_main
+
     def fwd():
         attnqat.check(lib.attnqat_quantize_qkv(pp, P(t["q"]), P(t["k"]), P(t["v"]), P(ws_f), ws_f.numel(), sp), "q")
-        attnqat.check(lib.attnqat_fwd_main(pp, P(o), P(o_hp), P(lse), P(ws_f), ws_f.numel(), sp), "fwd")
+        attnqat.check(fwd_main(pp, P(o), P(o_hp), P(lse), P(ws_f), ws_f.numel(), sp), "fwd")
 
     def bwd(ev=None):
         attnqat.check(lib.attnqat_bwd_preprocess(pp, P(t["do"]), P(t["q"]), P(t["k"]), P(t["v"]), P(o_hp),
@@ -433,11 +435,11 @@ def cpu_baseline(w, budget_s: float = 10.0) -> dict:
             f"backward {r['bwd_s']:.2f} s, forward {r['fwd_s']:.2f} s, float64 NumPy (BLAS on all cores)"}
 
 
-def workload_config(w, l2) -> dict:
+def workload_config(w, l2, recipe="standard") -> dict:
     return {"workload": f"{w.name}: B={w.B} H={w.H} Sq={w.Sq} Sk={w.Sk} D={w.D} "
             f"{'causal' if w.causal else 'non-causal'}, {w.structure} N(0,1) BF16, scale={w.scale:.6g}",
             "B": w.B, "H": w.H, "Sq": w.Sq, "Sk": w.Sk, "D": w.D, "causal": w.causal, "l2": l2,
-            "step": "quantize+fwd, then preprocess+bwd+dQ convert"}
+            "step": "quantize+fwd, then preprocess+bwd+dQ convert", "fwd_recipe": recipe}
 
 
 def main():
@@ -452,6 +454,9 @@ def main():
                     help="qat: the QAT forward+backward step; infer: the NVFP4 inference forward "
                          "(default: infer for ctx32k, qat otherwise)")
     ap.add_argument("--seq", type=int, default=None, help="override Sq = Sk of the workload (smaller captures)")
+    ap.add_argument("--recipe", default="standard", choices=["standard", "r2"],
+                    help="forward recipe of the QAT step: standard (two passes, P^ of the normalised P) or r2 "
+                         "(one pass, P^ of each key tile's unnormalised P)")
     args = ap.parse_args()
     w = synth.workload(args.workload) if args.seq is None else synth.workload(args.workload, Sq=args.seq,
                                                                                Sk=args.seq)
@@ -547,7 +552,7 @@ def main():
         "metric": METRIC,
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": r["step_ms"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic", "config": workload_config(w, l2),
+        "dtype": "bf16", "data": "synthetic", "config": workload_config(w, l2, args.recipe),
         "fwd_tflops": job_tflops(flops_f, args.steps, world, r["fwd_ms"]),
         "step_tflops": world * (flops_f + flops_b) / (r["step_ms"] * 1e-3) / 1e12,
         "bwd_ms": r["bwd_ms"] / args.steps, "fwd_ms": r["fwd_ms"] / args.steps,
