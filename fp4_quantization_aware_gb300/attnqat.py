@@ -57,6 +57,7 @@ SIGNATURES = {
     "attnqat_device_status": (_S, [ctypes.c_int]),
     "attnqat_selftest_wait_timeout": (_S, [ctypes.c_uint64, _P]),
     "attnqat_selftest_quotient": (_S, [_P, _P]),
+    "attnqat_selftest_scale": (_S, [_P, _P]),
     "attnqat_nvfp4_pack": (_S, [_P, _P, _P, ctypes.c_int64, ctypes.c_int64, _P]),
     "attnqat_infer_fwd_workspace_bytes": (ctypes.c_size_t, [_PP]),
     "attnqat_infer_fwd_packed": (_S, [_PP, _P, _P, _P, _P, _P, _P, _P, _P]),

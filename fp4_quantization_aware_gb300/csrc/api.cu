@@ -454,6 +454,12 @@ attnqat_status attnqat_selftest_quotient(unsigned long long* out, void* stream) 
   return ATTNQAT_OK;
 }
 
+attnqat_status attnqat_selftest_scale(unsigned long long* out, void* stream) {
+  ATTNQAT_TRY(check_ptrs({out}));
+  ATTNQAT_CUDA(launch_scale_selftest(out, static_cast<cudaStream_t>(stream)), "selftest_scale");
+  return ATTNQAT_OK;
+}
+
 attnqat_status attnqat_selftest_wait_timeout(uint64_t timeout_ns, void* stream) {
   attnqat_status st = ATTNQAT_OK;
   uint32_t* err = device_error_word(&st);

@@ -54,16 +54,6 @@ __device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity
   return ok != 0;
 }
 
-// Fake-quantize 16 probabilities (read-only copy) and pack the BF16 results.
-__device__ __forceinline__ void quant_pack16(const float* p, uint32_t* out8) {
-  float t[16];
-#pragma unroll
-  for (int k = 0; k < 16; ++k) t[k] = p[k];
-  fake_nvfp4_16(t);
-#pragma unroll
-  for (int k = 0; k < 8; ++k) out8[k] = pack_bf16x2(t[2 * k], t[2 * k + 1]);
-}
-
 // Store one thread's 64 packed BF16 values (32 words) as row `row` of the
 // 64-column block at `block_base`.
 __device__ __forceinline__ void store_row64(uint32_t block_base, uint32_t row, const uint32_t* w) {

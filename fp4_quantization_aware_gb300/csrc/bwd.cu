@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
 
       uint32_t ph[32];
 #pragma unroll
-      for (int g = 0; g < 4; ++g) quant_pack16(P + 16 * g, ph + 8 * g);
+      for (int g = 0; g < 4; ++g) fake_nvfp4_16_pack_nonneg<false>(P + 16 * g, 1.0f, ph + 8 * g);
       if (it > 0 && !warp_wait(&B.buf_free, (it - 1) & 1, ctl)) { ok = false; break; }
       store_row64(ps_block, r, ph);
       fence_proxy_async_smem();

@@ -364,7 +364,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
 #pragma unroll
       for (int k = 0; k < 32; ++k) pw[k] = pack_bf16x2(P[2 * k], P[2 * k + 1]);
 #pragma unroll
-      for (int g = 0; g < 4; ++g) quant_pack16(P + 16 * g, phw + 8 * g);
+      for (int g = 0; g < 4; ++g) fake_nvfp4_16_pack_nonneg<false>(P + 16 * g, 1.0f, phw + 8 * g);
       // over this warp's own (already read) S columns
       const uint32_t pcol = tmem + lane_off + L::kColS0 + s * 128 + half * 64;
       tmem_st32(pcol, pw);

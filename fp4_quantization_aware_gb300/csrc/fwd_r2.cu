@@ -82,17 +82,6 @@ struct R2Args {
   uint64_t timeout_ns;
 };
 
-// Fake-quantize 16 non-negative probabilities and pack the results, each
-// multiplied by `g`, as BF16 pairs.
-__device__ __forceinline__ void quant_scale_pack16(const float* p, float g, uint32_t* out8) {
-  float t[16];
-#pragma unroll
-  for (int k = 0; k < 16; ++k) t[k] = p[k];
-  fake_nvfp4_16(t);
-#pragma unroll
-  for (int k = 0; k < 8; ++k) out8[k] = pack_bf16x2(t[2 * k] * g, t[2 * k + 1] * g);
-}
-
 template <int D>
 __global__ void __launch_bounds__(kThreadsR2, 1)
     fwd_r2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -327,7 +316,7 @@ __global__ void __launch_bounds__(kThreadsR2, 1)
       }
       uint32_t phw[32];
 #pragma unroll
-      for (int g = 0; g < 4; ++g) quant_scale_pack16(pq + 16 * g, G, phw + 8 * g);
+      for (int g = 0; g < 4; ++g) fake_nvfp4_16_pack_nonneg<true>(pq + 16 * g, G, phw + 8 * g);
       tmem_st32(scol, pw);                                   // over this warp's own S columns
       tmem_st32(scol + 32, phw);
       tc_fence_before();

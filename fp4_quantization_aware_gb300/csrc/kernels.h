@@ -77,6 +77,7 @@ cudaError_t launch_infer(const Problem& p, const uint8_t* q_fp4, const uint8_t* 
                          const uint8_t* k_sf, const bf16* v, bf16* o, float* lse, uint32_t* err, cudaStream_t st);
 
 cudaError_t launch_quotient_selftest(unsigned long long* out, cudaStream_t st);
+cudaError_t launch_scale_selftest(unsigned long long* out, cudaStream_t st);
 
 cudaError_t launch_wait_timeout(uint32_t* err, uint64_t timeout_ns, cudaStream_t st);
 

@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(kThreads) quotient_selftest_kernel(unsigned lo
     const uint32_t lo = __float_as_uint(s * 0.125f);
     float a = __uint_as_float(lo + static_cast<uint32_t>(j % kQuotPerScale));
     if (i & 1) a = -a;
-    const float r = __frcp_rn(s);
+    const float r = rcp_scale(s);
     const float got = copysignf(div_by_scale(a, s, r), a);
     const float want = __fdiv_rn(a, s);
     if (__float_as_uint(got) != __float_as_uint(want)) {
@@ -223,6 +223,66 @@ __global__ void __launch_bounds__(kThreads) quotient_selftest_kernel(unsigned lo
     }
   }
   if (bad) atomicAdd(out, bad);
+}
+
+// The quantizer's scale arithmetic against IEEE arithmetic, and the packing
+// variant for non-negative inputs against the generic quantizer:
+//  out[0] (out[3]): FP32 amax in (kZeroScaleAmax, FLT_MAX] whose div6 differs
+//                   from __fdiv_rn(amax, 6) (the bits of one);
+//  out[1] (out[4]): positive E4M3 scales whose rcp_scale differs from __frcp_rn;
+//  out[2] (out[5]): pseudo-random groups of 16 non-negative values (zeros,
+//                   and magnitudes from 2^-23 to 2, so both paths run) whose
+//                   packed BF16 results differ from fake_nvfp4_16's (the index).
+constexpr int64_t kNonnegGroups = int64_t(1) << 24;
+
+__device__ __forceinline__ uint32_t mix32(uint32_t h) {   // an integer hash (xorshift-multiply rounds)
+  h ^= h >> 16, h *= 0x7feb352du;
+  h ^= h >> 15, h *= 0x846ca68bu;
+  return h ^ (h >> 16);
+}
+
+__global__ void __launch_bounds__(kThreads) scale_selftest_kernel(unsigned long long* out) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+  unsigned long long bad[3] = {0, 0, 0};
+  const uint32_t lo = __float_as_uint(kZeroScaleAmax) + 1u, hi = 0x7F7FFFFFu;
+  for (int64_t i = t0; i <= static_cast<int64_t>(hi - lo); i += stride) {
+    const float a = __uint_as_float(lo + static_cast<uint32_t>(i));
+    if (__float_as_uint(div6(a)) != __float_as_uint(__fdiv_rn(a, 6.0f))) {
+      ++bad[0];
+      atomicCAS(out + 3, 0ull, static_cast<unsigned long long>(__float_as_uint(a)) | 1ull << 32);
+    }
+  }
+  if (t0 < 126) {
+    const float sc = e4m3_value(1 + static_cast<int>(t0));
+    if (__float_as_uint(rcp_scale(sc)) != __float_as_uint(__frcp_rn(sc))) {
+      ++bad[1];
+      atomicCAS(out + 4, 0ull, static_cast<unsigned long long>(__float_as_uint(sc)) | 1ull << 32);
+    }
+  }
+  for (int64_t gi = t0; gi < kNonnegGroups; gi += stride) {
+    float x[16], y[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const uint32_t h = mix32(static_cast<uint32_t>(gi) * 16u + static_cast<uint32_t>(k) + 0x9e3779b9u);
+      const float v = ldexpf(1.0f + static_cast<float>(h & 0x7FFFFFu) * 0x1p-23f, -static_cast<int>((h >> 23) % 24u));
+      x[k] = (h >> 28) == 0u ? 0.0f : v;
+      y[k] = x[k];
+    }
+    fake_nvfp4_16(y);
+    uint32_t w[8];
+    fake_nvfp4_16_pack_nonneg<false>(x, 1.0f, w);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (w[k] != pack_bf16x2(y[2 * k], y[2 * k + 1])) {
+        ++bad[2];
+        atomicCAS(out + 5, 0ull, static_cast<unsigned long long>(gi) | 1ull << 40);
+        break;
+      }
+    }
+  }
+  for (int k = 0; k < 3; ++k)
+    if (bad[k]) atomicAdd(out + k, bad[k]);
 }
 
 inline unsigned blocks_for(int64_t n) { return static_cast<unsigned>((n + kThreads - 1) / kThreads); }
@@ -278,6 +338,11 @@ cudaError_t launch_dq_convert(const Problem& p, const float* dq_acc, bf16* dq, c
   const int64_t n4 = p.bh() * p.Sq * p.D / 4;
   dq_convert_kernel<<<blocks_for(n4), kThreads, 0, st>>>(reinterpret_cast<const float4*>(dq_acc),
                                                          reinterpret_cast<uint2*>(dq), n4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scale_selftest(unsigned long long* out, cudaStream_t st) {
+  scale_selftest_kernel<<<152 * 8, kThreads, 0, st>>>(out);
   return cudaGetLastError();
 }
 

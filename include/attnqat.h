@@ -227,6 +227,17 @@ attnqat_status attnqat_device_status(int clear);
  * division" requirement of the cuDNN page (Overview). */
 attnqat_status attnqat_selftest_quotient(unsigned long long* out, void* stream);
 
+/* Checks the quantizer's scale arithmetic and its packing variant for
+ * non-negative inputs, bit for bit: (0) the FMA-corrected amax / 6 against IEEE
+ * FP32 division for every FP32 amax above the zero-scale bound 6 * 2^-10;
+ * (1) the refined reciprocal against IEEE reciprocal for all 126 positive
+ * E4M3 scales; (2) the non-negative variant (the one the attention kernels
+ * apply to P) against the generic quantizer on 2^24 pseudo-random groups. `out`
+ * is a device pointer to 6 unsigned 64-bit words, written on `stream` and
+ * expected zero-initialised: the three mismatch counts, then an example of
+ * each (bits of amax, bits of the scale, group index; bit 32 or 40 set). */
+attnqat_status attnqat_selftest_scale(unsigned long long* out, void* stream);
+
 /* Launches one CTA that waits on a barrier that nothing arrives at, with a
  * limit of timeout_ns nanoseconds; it then records ATTNQAT_ERR_TIMEOUT in the
  * device error word and returns. Exercises the bounded-wait path without

@@ -128,3 +128,19 @@ def test_quotient_matches_ieee_division_exhaustively(lib):
     torch.cuda.synchronize()
     n, a_bits, s_bits = out.cpu().tolist()
     assert n == 0, f"{n} mismatches, e.g. a bits {a_bits & 0xFFFFFFFF:#x}, s bits {s_bits:#x}"
+
+
+def test_scale_arithmetic_and_nonneg_variant_exhaustively(lib):
+    """amax / 6 by FMA correction equals IEEE division for every FP32 amax that
+    reaches it; the refined reciprocal equals IEEE reciprocal on every E4M3
+    scale; the attention kernels' variant for probabilities equals the generic
+    quantizer bit for bit."""
+    import torch
+    out = torch.zeros(6, dtype=torch.int64, device="cuda")
+    attnqat.check(lib.attnqat_selftest_scale(out.data_ptr(), torch.cuda.current_stream().cuda_stream),
+                  "selftest_scale")
+    torch.cuda.synchronize()
+    n_div, n_rcp, n_quant, e_div, e_rcp, e_quant = out.cpu().tolist()
+    assert n_div == 0, f"{n_div} amax / 6 mismatches, e.g. amax bits {e_div & 0xFFFFFFFF:#x}"
+    assert n_rcp == 0, f"{n_rcp} reciprocal mismatches, e.g. scale bits {e_rcp & 0xFFFFFFFF:#x}"
+    assert n_quant == 0, f"{n_quant} group mismatches, e.g. group {e_quant & 0xFFFFFFFFFF}"
