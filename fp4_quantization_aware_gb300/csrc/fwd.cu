@@ -20,17 +20,22 @@
 // put P in columns 64h + [0,32) and P^ in 64h + [32,64) of that S buffer,
 // columns only they read, and the O' and O MMAs take their A operand from
 // TMEM there. The next S goes into a buffer once the MMAs reading its P are
-// done. Warp roles (10 warps): 0-7 softmax (warp w: lanes 32*(w%4).., key
-// columns [64*(w/4), +64)); 8 TMA producer; 9 MMA issuer.
-// Shared memory (D = 128): Q^ 32K, K^ x2 64K, V^ x2 64K, NVFP4 Q 8K, NVFP4 K x2 16K.
+// done (issue order). Warp roles (10 warps): 0-7 softmax (warp w: lanes
+// 32*(w%4).., key columns [64*(w/4), +64)); 8 TMA producer; 9 MMA issuer.
+// K^ and V^ tiles are triple-buffered in shared memory.
 //
-// Pass 1 at D = 128 computes S on the block-scaled NVFP4 tensor-core MMA
+// D = 128: both passes compute S on the block-scaled NVFP4 tensor-core MMA
 // (2 MMAs of K = 64 per tile instead of 8 BF16 ones) from the NVFP4 encoding
-// of Q and K, whose values are exactly Q^ and K^. Its scale factors sit in
-// the O' columns, which pass 1 does not use: Q scales at O' + [0,8), K scales
-// of tile t at O' + 16 + 16 (t % 2) + [0,8). The softmax warps write tile
-// t + 2's K scales once S(t) is complete, before releasing S(t); the first O'
-// MMA of pass 2 runs after every pass-1 MMA (issue order).
+// of Q and K, whose values are exactly Q^ and K^. The MMA's scale factors sit
+// in TMEM. For pass 1 and the first two pass-2 tiles they are in the O'
+// columns, which hold no accumulator yet: Q at O' + [0,8), K of tile t at
+// O' + 16 + 16 (t % 2) + [0,8). For a later pass-2 tile t + 1 they are in
+// columns 64h + [32,40) of S(t)'s buffer (K step h), written by the softmax
+// warps of half h as soon as they have read S(t); those warps write the first
+// 8 P^ columns of tile t there once S(t + 1) is complete. Shared memory:
+// V^ x3 96K, NVFP4 Q 8K, NVFP4 K x3 24K.
+// D = 64: S on BF16 MMAs from Q^, K^ in both passes. Shared memory: V^ x3,
+// Q^, K^ x3.
 #include "attn_common.cuh"
 #include "fp4_mma.cuh"
 
@@ -43,35 +48,39 @@ constexpr int kWarpMmaF = 9;
 
 template <int D>
 struct FwdLayout {
-  static constexpr bool kFp4 = D == 128;                 // pass 1 on the block-scaled NVFP4 MMA
+  static constexpr bool kFp4 = D == 128;                 // S on the block-scaled NVFP4 MMA
   static constexpr uint32_t kTile = 128 * D * 2;
   static constexpr uint32_t kFp4Tile = 128 * 64;         // 128 rows x 64 bytes of E2M1 pairs
-  static constexpr uint32_t kQ = 0;
+  static constexpr int kStages = 3;                     // K and V tiles in flight
+  static constexpr uint32_t kV0 = 0;                     // V^ stage s at kV0 + s * kTile
+  // D = 64: BF16 Q^, K^ (stage s at kK0 + s * kTile)
+  static constexpr uint32_t kQ = kV0 + kStages * kTile;
   static constexpr uint32_t kK0 = kQ + kTile;
-  static constexpr uint32_t kK1 = kK0 + kTile;
-  static constexpr uint32_t kV0 = kK1 + kTile;
-  static constexpr uint32_t kV1 = kV0 + kTile;
-  static constexpr uint32_t kQ4 = kV1 + kTile;
+  // D = 128: NVFP4 Q, K (stage s at kK40 + s * kFp4Tile)
+  static constexpr uint32_t kQ4 = kV0 + kStages * kTile;
   static constexpr uint32_t kK40 = kQ4 + kFp4Tile;
-  static constexpr uint32_t kK41 = kK40 + kFp4Tile;
-  static constexpr uint32_t kML = kFp4 ? kK41 + kFp4Tile : kQ4;   // 128 rows x (m, l) of half 1, then 128 lse2
+  static constexpr uint32_t kML = kFp4 ? kK40 + kStages * kFp4Tile : kK0 + kStages * kTile;   // (m, l) of half 1, lse2
   static constexpr uint32_t kBar = kML + 1536;
   static constexpr uint32_t kBytes = kBar + 256;
   static constexpr uint32_t kAlloc = kBytes + 1024;
   static constexpr uint32_t kColS0 = 0;
   static constexpr uint32_t kColOP = 256;
   static constexpr uint32_t kColO = 256 + D;
-  static constexpr uint32_t kColSFQ = kColOP;            // pass 1 only
+  static constexpr uint32_t kColSFQ = kColOP;            // pass 1 and pass-2 tiles 0, 1
   static constexpr uint32_t kColSFK0 = kColOP + 16;
   static constexpr uint32_t kColSFK1 = kColOP + 32;
+  static constexpr uint32_t kColSFQ2 = 32;               // later pass-2 tiles: + 128 * buffer + 64 * ks
+  static constexpr uint32_t kColSFK2 = 36;
+  static_assert(kColSFQ2 % 4 == 0 && kColSFK2 == kColSFQ2 + 4 && kColSFK2 + 4 <= 64,
+                "pass-2 scale factors: 4-column aligned, inside the free half of a key half's columns");
 };
 
 struct FwdBars {
   uint64_t q_full;
-  uint64_t k_full[2];
-  uint64_t k_empty[2];
-  uint64_t v_full[2];
-  uint64_t v_empty[2];
+  uint64_t k_full[3];    // per K / V stage
+  uint64_t k_empty[3];
+  uint64_t v_full[3];
+  uint64_t v_empty[3];
   uint64_t s_full[2];
   uint64_t s_free[2];
   uint64_t p_ready[2];   // per S buffer: P and P^ of a pass-2 tile are in TMEM
@@ -121,11 +130,11 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
   if (threadIdx.x == 0) {
     B.abort_flag = 0;
     mbar_init(&B.q_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < L::kStages; ++s) {
       mbar_init(&B.k_full[s], 1), mbar_init(&B.k_empty[s], 1);
       mbar_init(&B.v_full[s], 1), mbar_init(&B.v_empty[s], 1);
-      mbar_init(&B.s_full[s], 1), mbar_init(&B.s_free[s], 256);
     }
+    for (int s = 0; s < 2; ++s) mbar_init(&B.s_full[s], 1), mbar_init(&B.s_free[s], 256);
     mbar_init(&B.p_ready[0], 256);
     mbar_init(&B.p_ready[1], 256);
     mbar_init(&B.o_done, 1);
@@ -150,35 +159,39 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tm_q), tma_prefetch_desc(&tm_k), tma_prefetch_desc(&tm_v);
       if (L::kFp4) tma_prefetch_desc(&tm_q4), tma_prefetch_desc(&tm_k4);
-      int k_uses[2] = {0, 0}, v_uses[2] = {0, 0};
-      mbar_arrive_expect_tx(&B.q_full, L::kTile + (L::kFp4 ? L::kFp4Tile : 0));
-      for (int b = 0; b < D / 64; ++b)
-        tma_load_3d(smem + L::kQ + b * kBlockBytes, &tm_q, &B.q_full, b * 64, i * 128, bh);
-      if (L::kFp4) tma_load_3d(smem + L::kQ4, &tm_q4, &B.q_full, 0, i * 128, bh);
+      int k_uses[L::kStages] = {}, v_uses[L::kStages] = {};
+      if constexpr (L::kFp4) {                          // NVFP4 Q only
+        mbar_arrive_expect_tx(&B.q_full, L::kFp4Tile);
+        tma_load_3d(smem + L::kQ4, &tm_q4, &B.q_full, 0, i * 128, bh);
+      } else {
+        mbar_arrive_expect_tx(&B.q_full, L::kTile);
+        for (int b = 0; b < D / 64; ++b)
+          tma_load_3d(smem + L::kQ + b * kBlockBytes, &tm_q, &B.q_full, b * 64, i * 128, bh);
+      }
       for (int t = 0; t < nt; ++t) {
         const int jt = t < nk ? t : t - nk;
-        const int s = t & 1;
-        if (t >= 2 && !mbar_wait(&B.k_empty[s], ((t >> 1) - 1) & 1, ctl)) break;
-        if (L::kFp4 && t < nk) {                          // pass 1: NVFP4 K
+        const int s = t % L::kStages, use = t / L::kStages;
+        if (use >= 1 && !mbar_wait(&B.k_empty[s], (use - 1) & 1, ctl)) break;
+        if constexpr (L::kFp4) {                           // NVFP4 K in both passes
           mbar_arrive_expect_tx(&B.k_full[s], L::kFp4Tile);
-          tma_load_3d(smem + (s ? L::kK41 : L::kK40), &tm_k4, &B.k_full[s], 0, jt * 128, bh);
+          tma_load_3d(smem + L::kK40 + s * L::kFp4Tile, &tm_k4, &B.k_full[s], 0, jt * 128, bh);
         } else {
           mbar_arrive_expect_tx(&B.k_full[s], L::kTile);
           for (int b = 0; b < D / 64; ++b)
-            tma_load_3d(smem + (s ? L::kK1 : L::kK0) + b * kBlockBytes, &tm_k, &B.k_full[s], b * 64, jt * 128, bh);
+            tma_load_3d(smem + L::kK0 + s * L::kTile + b * kBlockBytes, &tm_k, &B.k_full[s], b * 64, jt * 128, bh);
         }
         ++k_uses[s];
         if (t >= nk) {
-          const int tv = t - nk, sv = tv & 1;
-          if (tv >= 2 && !mbar_wait(&B.v_empty[sv], ((tv >> 1) - 1) & 1, ctl)) break;
+          const int tv = t - nk, sv = tv % L::kStages, vuse = tv / L::kStages;
+          if (vuse >= 1 && !mbar_wait(&B.v_empty[sv], (vuse - 1) & 1, ctl)) break;
           mbar_arrive_expect_tx(&B.v_full[sv], L::kTile);
           for (int b = 0; b < D / 64; ++b)
-            tma_load_3d(smem + (sv ? L::kV1 : L::kV0) + b * kBlockBytes, &tm_v, &B.v_full[sv], b * 64, jt * 128, bh);
+            tma_load_3d(smem + L::kV0 + sv * L::kTile + b * kBlockBytes, &tm_v, &B.v_full[sv], b * 64, jt * 128, bh);
           ++v_uses[sv];
         }
       }
       mbar_wait_drain(&B.q_full, 0, ctl);
-      for (int s = 0; s < 2; ++s) {
+      for (int s = 0; s < L::kStages; ++s) {
         if (k_uses[s]) mbar_wait_drain(&B.k_full[s], (k_uses[s] - 1) & 1, ctl);
         if (v_uses[s]) mbar_wait_drain(&B.v_full[s], (v_uses[s] - 1) & 1, ctl);
       }
@@ -192,10 +205,9 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       // instructions per MMA for a thread that shares its sub-partition).
       const uint64_t kmaj = sdesc_sw128(sbase, 16, 1024);
       const uint64_t mnmaj = sdesc_sw128(sbase, kBlockBytes, 1024);
-      const uint64_t dq = sdesc_advance(kmaj, L::kQ);
       auto issue_s = [&](int t) -> bool {
-        const int s = t & 1;
-        if (!mbar_wait(&B.k_full[s], (t >> 1) & 1, ctl)) return false;
+        const int s = t & 1, ks_ = t % L::kStages;
+        if (!mbar_wait(&B.k_full[ks_], (t / L::kStages) & 1, ctl)) return false;
         // The buffer's previous tile u = t - 2 must be done with. A pass-1 S is
         // done once the softmax warps have read it. A pass-2 buffer holds P(u),
         // which the O' and O MMAs of tile u read; those were issued by this
@@ -204,16 +216,24 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         // running instead of draining once per tile).
         const int u = t - 2;
         if (u >= 0 && u < nk && !mbar_wait(&B.s_free[s], (u >> 1) & 1, ctl)) return false;
+        // D = 128, pass-2 tiles from the third on: the scale factors are in the
+        // previous tile's S buffer, written there once the softmax warps have
+        // read that S (they arrive on its s_free in both passes).
+        const bool sf_in_s = L::kFp4 && t >= nk + 2;
+        if (sf_in_s && !mbar_wait(&B.s_free[(t - 1) & 1], ((t - 1) >> 1) & 1, ctl)) return false;
         tc_fence_after();
-        if (L::kFp4 && t < nk) {
-          const uint64_t d4q = sdesc_sw64(sbase + L::kQ4), d4k = sdesc_sw64(sbase + (s ? L::kK41 : L::kK40));
-          const uint32_t sfk = s ? L::kColSFK1 : L::kColSFK0;
+        if constexpr (L::kFp4) {
+          const uint64_t d4q = sdesc_sw64(sbase + L::kQ4), d4k = sdesc_sw64(sbase + L::kK40 + ks_ * L::kFp4Tile);
+          const uint32_t sfq = sf_in_s ? L::kColS0 + ((t - 1) & 1) * 128 + L::kColSFQ2 : L::kColSFQ;
+          const uint32_t sfk = sf_in_s ? L::kColS0 + ((t - 1) & 1) * 128 + L::kColSFK2 : (s ? L::kColSFK1 : L::kColSFK0);
+          const uint32_t step = sf_in_s ? 64u : 4u;      // column distance between the K = 64 steps' factors
 #pragma unroll
           for (int ks = 0; ks < 2; ++ks)
             umma_nvfp4(tmem + L::kColS0 + s * 128, sdesc_advance(d4q, ks * 32), sdesc_advance(d4k, ks * 32),
-                       idesc_nvfp4(128, 128), tmem + L::kColSFQ + ks * 4, tmem + sfk + ks * 4, ks > 0);
+                       idesc_nvfp4(128, 128), tmem + sfq + ks * step, tmem + sfk + ks * step, ks > 0);
         } else {
-          const uint64_t db = sdesc_advance(kmaj, s ? L::kK1 : L::kK0);
+          const uint64_t dq = sdesc_advance(kmaj, L::kQ);
+          const uint64_t db = sdesc_advance(kmaj, L::kK0 + ks_ * L::kTile);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t o = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
@@ -221,7 +241,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
           }
         }
         umma_commit(&B.s_full[s]);
-        umma_commit(&B.k_empty[s]);
+        umma_commit(&B.k_empty[ks_]);
         return true;
       };
       // O (+)= A[128 q x 128 keys] V^[128 keys x D]: A from TMEM at `a_col`
@@ -239,14 +259,14 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       for (int t = 0; ok && t < nt; ++t) {
         if (t + 1 < nt && !issue_s(t + 1)) break;
         if (t >= nk) {
-          const int tv = t - nk, sv = tv & 1;
-          if (!mbar_wait(&B.v_full[sv], (tv >> 1) & 1, ctl)) break;
+          const int tv = t - nk, sv = tv % L::kStages;
+          if (!mbar_wait(&B.v_full[sv], (tv / L::kStages) & 1, ctl)) break;
           // use index of this tile's S buffer among pass-2 tiles (one barrier
           // per buffer, so the softmax warps running ahead cannot alias phases)
           const int pr_use = (t >> 1) - ((nk + 1 - (t & 1)) >> 1);
           if (!mbar_wait(&B.p_ready[t & 1], pr_use & 1, ctl)) break;
           tc_fence_after();
-          const uint32_t vb = sv ? L::kV1 : L::kV0;
+          const uint32_t vb = L::kV0 + sv * L::kTile;
           const uint32_t sc = L::kColS0 + (t & 1) * 128;
           mma_pv(sc, vb, L::kColOP, tv > 0);        // O' += P V^
           mma_pv(sc + 32, vb, L::kColO, tv > 0);    // O  += P^ V^
@@ -272,50 +292,61 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       tmem_st4(tmem + lane_off + L::kColSFQ + 4 * half, w);
       load_scales(a.k_sf, kbase, min(128, a.Sk), half, w);
       tmem_st4(tmem + lane_off + L::kColSFK0 + 4 * half, w);
-      if (nk > 1) {
-        load_scales(a.k_sf, kbase + 128, min(128, a.Sk - 128), half, w);
-        tmem_st4(tmem + lane_off + L::kColSFK1 + 4 * half, w);
-      }
+      const int kt1 = nk > 1 ? 1 : 0;   // tile 1 is pass 2's first when nk = 1
+      load_scales(a.k_sf, kbase + kt1 * 128, min(128, a.Sk - kt1 * 128), half, w);
+      tmem_st4(tmem + lane_off + L::kColSFK1 + 4 * half, w);
       tc_fence_before();
       mbar_arrive(&B.sf_init);
     }
 
     // pass 1: running max and sum of exp2(S * c2) over this thread's key columns
+    const float2 c22 = make_float2(a.c2, a.c2);
     float m = -INFINITY, l = 0.0f;
     for (int t = 0; t < nk; ++t) {
       const int s = t & 1;
       const int valid = kend - (t * 128 + static_cast<int>(half) * 64);
-      const bool more = L::kFp4 && t + 2 < nk;
+      // K scales of tile t + 2 (up to pass 2's second tile, key tile 1)
+      const bool more = L::kFp4 && t + 2 < nt;
+      const int kt2 = t + 2 < nk ? t + 2 : t + 2 - nk;
       uint32_t sfw[4] = {0u, 0u, 0u, 0u};
-      if (more) load_scales(a.k_sf, kbase + (t + 2) * 128, min(128, a.Sk - (t + 2) * 128), half, sfw);
+      if (more) load_scales(a.k_sf, kbase + kt2 * 128, min(128, a.Sk - kt2 * 128), half, sfw);
       if (!warp_wait(&B.s_full[s], (t >> 1) & 1, ctl)) { ok = false; break; }
       tc_fence_after();
-      float x[64];
-      {
-        uint32_t v[64];
-        tmem_ld64(tmem + lane_off + L::kColS0 + s * 128 + half * 64, v);
-#pragma unroll
-        for (int k = 0; k < 64; ++k) x[k] = (k < valid) ? __uint_as_float(v[k]) * a.c2 : -INFINITY;
-      }
-      // tile t + 2's K scales into the buffer S(t) used (S(t) is complete);
+      uint32_t v[64];
+      tmem_ld64(tmem + lane_off + L::kColS0 + s * 128 + half * 64, v);
+      // tile t + 2's K scales into the slot S(t) used (S(t) is complete);
       // releasing S(t) below also certifies them to the MMA issuer
       if (more) tmem_st4(tmem + lane_off + (s ? L::kColSFK1 : L::kColSFK0) + 4 * half, sfw);
       tc_fence_before();
       mbar_arrive(&B.s_free[s]);
-      // four independent chains for the row max and the row sum (ILP)
-      float mc[4] = {m, m, m, m};
+      if (valid < 64) {   // masked keys: -inf
 #pragma unroll
-      for (int k = 0; k < 64; k += 4)
+        for (int k = 0; k < 64; ++k)
+          if (k >= valid) v[k] = 0xFF800000u;
+      }
+      // Row max of the raw S (four chains of 3-input max); c2 > 0 and rounding
+      // is monotonic, so max(S) * c2 is the max of the scaled logits.
+      float mq[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) mc[u] = fmaxf(mc[u], x[k + u]);
-      const float mx = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3]));
+      for (int u = 0; u < 4; ++u) {
+        float acc = fmaxf(__uint_as_float(v[16 * u]), __uint_as_float(v[16 * u + 1]));
+#pragma unroll
+        for (int k = 2; k < 16; k += 2) acc = fmax3(acc, __uint_as_float(v[16 * u + k]), __uint_as_float(v[16 * u + k + 1]));
+        mq[u] = acc;
+      }
+      const float mx = fmaxf(m, fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * a.c2);
       if (mx == -INFINITY) continue;
-      float sc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      // sum of exp2(S * c2 - mx), arguments and partial sums as packed pairs
+      const float2 nm = make_float2(-mx, -mx);
+      float2 sc[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
+                      make_float2(0.0f, 0.0f)};
 #pragma unroll
-      for (int k = 0; k < 64; k += 4)
-#pragma unroll
-        for (int u = 0; u < 4; ++u) sc[u] += ex2(x[k + u] - mx);
-      l = l * ex2(m - mx) + ((sc[0] + sc[1]) + (sc[2] + sc[3]));
+      for (int k = 0; k < 32; ++k) {
+        const float2 e = ffma2(make_float2(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1])), c22, nm);
+        sc[k & 3] = fadd2(sc[k & 3], make_float2(ex2(e.x), ex2(e.y)));
+      }
+      const float2 st = fadd2(fadd2(sc[0], sc[1]), fadd2(sc[2], sc[3]));
+      l = l * ex2(m - mx) + (st.x + st.y);
       m = mx;
     }
     // Combine the two column halves of each row: half 1 hands (m, l) to half
@@ -345,30 +376,66 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     }
 
     // pass 2: P = exp2(S * c2 - lse2), P^ = fake_nvfp4(P); hand both to the MMA warp
+    const int64_t qsf_row0 = static_cast<int64_t>(bh) * a.Sq + i * 128;
+    const int qsf_rows = min(128, a.Sq - i * 128);
     for (int t = nk; ok && t < nt; ++t) {
       const int s = t & 1, tv = t - nk;
       const int valid = kend - (tv * 128 + static_cast<int>(half) * 64);
+      // D = 128: this warp puts the scale factors of S(t + 1) (pass-2 tiles
+      // from the third on; K step `half`) into S(t)'s buffer, where its P^
+      // columns [32,40) go later
+      const bool wsf = L::kFp4 && tv >= 1 && t + 1 < nt;
+      uint32_t sfq[4] = {0u, 0u, 0u, 0u}, sfk[4] = {0u, 0u, 0u, 0u};
+      if (wsf) {
+        load_scales(a.q_sf, qsf_row0, qsf_rows, half, sfq);
+        load_scales(a.k_sf, kbase + (tv + 1) * 128, min(128, a.Sk - (tv + 1) * 128), half, sfk);
+      }
       if (!warp_wait(&B.s_full[s], (t >> 1) & 1, ctl)) { ok = false; break; }
       tc_fence_after();
+      const uint32_t pcol = tmem + lane_off + L::kColS0 + s * 128 + half * 64;   // this warp's S columns
       float P[64];
       {
         uint32_t v[64];
-        tmem_ld64(tmem + lane_off + L::kColS0 + s * 128 + half * 64, v);
-#pragma unroll
-        for (int k = 0; k < 64; ++k) {
-          const float p = ex2(fmaf(__uint_as_float(v[k]), a.c2, -lse2));
-          P[k] = (k < valid) ? p : 0.0f;
+        tmem_ld64(pcol, v);
+        if constexpr (L::kFp4) {   // S(t) is read: scale factors of S(t + 1), then release it
+          if (wsf) {
+            tmem_st4(pcol + L::kColSFQ2, sfq);
+            tmem_st4(pcol + L::kColSFK2, sfk);
+          }
+          tc_fence_before();
+          mbar_arrive(&B.s_free[s]);
         }
+        const float2 nl = make_float2(-lse2, -lse2);
+#pragma unroll
+        for (int k = 0; k < 64; k += 2) {
+          const float2 e = ffma2(make_float2(__uint_as_float(v[k]), __uint_as_float(v[k + 1])), c22, nl);
+          P[k] = ex2(e.x), P[k + 1] = ex2(e.y);
+        }
+      }
+      if (valid < 64) {   // masked keys: P = 0
+#pragma unroll
+        for (int k = 0; k < 64; ++k)
+          if (k >= valid) P[k] = 0.0f;
       }
       uint32_t pw[32], phw[32];
 #pragma unroll
       for (int k = 0; k < 32; ++k) pw[k] = pack_bf16x2(P[2 * k], P[2 * k + 1]);
 #pragma unroll
       for (int g = 0; g < 4; ++g) fake_nvfp4_16_pack_nonneg<false>(P + 16 * g, 1.0f, phw + 8 * g);
-      // over this warp's own (already read) S columns
-      const uint32_t pcol = tmem + lane_off + L::kColS0 + s * 128 + half * 64;
+      // P over columns [0,32) of this warp's S columns, P^ over [32,64)
       tmem_st32(pcol, pw);
-      tmem_st32(pcol + 32, phw);
+      if (wsf) {
+        // P^ columns [32,40) hold the scale factors of S(t + 1): write them once it is complete
+        tmem_st16_nowait(pcol + 40, phw + 8);
+        tmem_st8_nowait(pcol + 56, phw + 24);
+        tmem_wait_st();
+        if (!warp_wait(&B.s_full[(t + 1) & 1], ((t + 1) >> 1) & 1, ctl)) { ok = false; break; }
+        tc_fence_after();
+        tmem_st8_nowait(pcol + 32, phw);
+        tmem_wait_st();
+      } else {
+        tmem_st32(pcol + 32, phw);
+      }
       tc_fence_before();
       mbar_arrive(&B.p_ready[s]);
     }

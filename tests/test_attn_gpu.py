@@ -25,6 +25,7 @@ CASES = [
     (1, 1, 300, 129, 64, False, 2.0),
     (1, 2, 384, 384, 128, True, 2.0),      # several causal tiles
     (1, 1, 520, 520, 64, True, 3.0),       # tail of 8 rows past four tiles
+    (1, 2, 200, 1000, 128, False, 3.0),    # eight key tiles with a ragged last one
 ]
 
 
