@@ -289,6 +289,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         dlt_out = __ldg(a.delta + (size_t)bh * a.Sq + row);
       }
     };
+    const float2 c22 = make_float2(a.c2, a.c2);
     float lse_next, dlt_next;
     row_stats(0, lse_next, dlt_next);
     for (int it = 0; it < n_it; ++it) {
@@ -305,11 +306,17 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       {
         uint32_t v[64];
         tmem_ld64(tmem + lane_off + s_region(it) + half * 64, v);
+        const float2 nl = make_float2(-lse2, -lse2);
 #pragma unroll
-        for (int k = 0; k < 64; ++k) {
-          const float p = ex2(fmaf(__uint_as_float(v[k]), a.c2, -lse2));
-          P[k] = (k < valid) ? p : 0.0f;
+        for (int k = 0; k < 64; k += 2) {
+          const float2 e = ffma2(make_float2(__uint_as_float(v[k]), __uint_as_float(v[k + 1])), c22, nl);
+          P[k] = ex2(e.x), P[k + 1] = ex2(e.y);
         }
+      }
+      if (valid < 64) {   // masked keys: P = 0
+#pragma unroll
+        for (int k = 0; k < 64; ++k)
+          if (k >= valid) P[k] = 0.0f;
       }
       tc_fence_before();
       mbar_arrive(&B.s_free);
@@ -328,11 +335,12 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       {
         uint32_t v[64];
         tmem_ld64(tmem + lane_off + dp_region(it) + half * 64, v);
+        const float2 ndl = make_float2(-dlt, -dlt);
 #pragma unroll
         for (int k = 0; k < 64; k += 2) {
-          const float d0 = P[k] * (__uint_as_float(v[k]) - dlt);
-          const float d1 = P[k + 1] * (__uint_as_float(v[k + 1]) - dlt);
-          ds[k / 2] = pack_bf16x2(d0, d1);
+          const float2 d = fmul2(make_float2(P[k], P[k + 1]),
+                                 fadd2(make_float2(__uint_as_float(v[k]), __uint_as_float(v[k + 1])), ndl));
+          ds[k / 2] = pack_bf16x2(d.x, d.y);
         }
       }
       tc_fence_before();

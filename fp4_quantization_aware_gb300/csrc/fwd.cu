@@ -69,10 +69,12 @@ struct FwdLayout {
   static constexpr uint32_t kColSFQ = kColOP;            // pass 1 and pass-2 tiles 0, 1
   static constexpr uint32_t kColSFK0 = kColOP + 16;
   static constexpr uint32_t kColSFK1 = kColOP + 32;
-  static constexpr uint32_t kColSFQ2 = 32;               // later pass-2 tiles: + 128 * buffer + 64 * ks
-  static constexpr uint32_t kColSFK2 = 36;
-  static_assert(kColSFQ2 % 4 == 0 && kColSFK2 == kColSFQ2 + 4 && kColSFK2 + 4 <= 64,
-                "pass-2 scale factors: 4-column aligned, inside the free half of a key half's columns");
+  // later pass-2 tiles: + 128 * buffer + 64 * ks, over the P^ columns of the
+  // key half's last 16 keys (read by the last O MMA of that half)
+  static constexpr uint32_t kColSFQ2 = 56;
+  static constexpr uint32_t kColSFK2 = 60;
+  static_assert(kColSFQ2 % 4 == 0 && kColSFK2 == kColSFQ2 + 4 && kColSFK2 + 4 == 64,
+                "pass-2 scale factors: 4-column aligned, over the last 8 P^ columns of a key half");
 };
 
 struct FwdBars {
@@ -83,7 +85,8 @@ struct FwdBars {
   uint64_t v_empty[3];
   uint64_t s_full[2];
   uint64_t s_free[2];
-  uint64_t p_ready[2];   // per S buffer: P and P^ of a pass-2 tile are in TMEM
+  uint64_t p_ready[2];   // per S buffer: P and P^ of a pass-2 tile are in TMEM, but for
+  uint64_t p_late[2];    // the P^ columns of each key half's last 16 keys
   uint64_t o_done;       // one phase: every O' and O MMA has completed
   uint64_t ml_ready;
   uint64_t lse_ready;
@@ -137,6 +140,8 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     for (int s = 0; s < 2; ++s) mbar_init(&B.s_full[s], 1), mbar_init(&B.s_free[s], 256);
     mbar_init(&B.p_ready[0], 256);
     mbar_init(&B.p_ready[1], 256);
+    mbar_init(&B.p_late[0], 256);
+    mbar_init(&B.p_late[1], 256);
     mbar_init(&B.o_done, 1);
     mbar_init(&B.ml_ready, 128);
     mbar_init(&B.lse_ready, 128);
@@ -269,7 +274,26 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
           const uint32_t vb = L::kV0 + sv * L::kTile;
           const uint32_t sc = L::kColS0 + (t & 1) * 128;
           mma_pv(sc, vb, L::kColOP, tv > 0);        // O' += P V^
-          mma_pv(sc + 32, vb, L::kColO, tv > 0);    // O  += P^ V^
+          // O += P^ V^: the k-steps of each key half's last 16 keys go last,
+          // once their P^ columns are written (they may have held the scale
+          // factors of the next S)
+          {
+            const uint64_t dv = sdesc_advance(mnmaj, vb);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              if ((kk & 3) == 3) continue;
+              const uint32_t ac = sc + 32 + (kk >> 2) * 64 + (kk & 3) * 8;
+              umma_bf16_tmem_a(tmem + L::kColO, tmem + ac, sdesc_advance(dv, kk * 2048), kIdO,
+                               (tv > 0 || kk > 0) ? 1u : 0u);
+            }
+            if (!mbar_wait(&B.p_late[t & 1], pr_use & 1, ctl)) break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 3; kk < 8; kk += 4) {
+              const uint32_t ac = sc + 32 + (kk >> 2) * 64 + (kk & 3) * 8;
+              umma_bf16_tmem_a(tmem + L::kColO, tmem + ac, sdesc_advance(dv, kk * 2048), kIdO, 1u);
+            }
+          }
           umma_commit(&B.v_empty[sv]);
           if (tv == nk - 1) umma_commit(&B.o_done);
         }
@@ -376,8 +400,8 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     }
 
     // pass 2: P = exp2(S * c2 - lse2), P^ = fake_nvfp4(P); hand both to the MMA warp
-    const int64_t qsf_row0 = static_cast<int64_t>(bh) * a.Sq + i * 128;
-    const int qsf_rows = min(128, a.Sq - i * 128);
+    uint32_t sfq[4] = {0u, 0u, 0u, 0u};   // D = 128: this half's K step of the Q scale factors
+    if (L::kFp4) load_scales(a.q_sf, static_cast<int64_t>(bh) * a.Sq + i * 128, min(128, a.Sq - i * 128), half, sfq);
     for (int t = nk; ok && t < nt; ++t) {
       const int s = t & 1, tv = t - nk;
       const int valid = kend - (tv * 128 + static_cast<int>(half) * 64);
@@ -385,11 +409,8 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       // from the third on; K step `half`) into S(t)'s buffer, where its P^
       // columns [32,40) go later
       const bool wsf = L::kFp4 && tv >= 1 && t + 1 < nt;
-      uint32_t sfq[4] = {0u, 0u, 0u, 0u}, sfk[4] = {0u, 0u, 0u, 0u};
-      if (wsf) {
-        load_scales(a.q_sf, qsf_row0, qsf_rows, half, sfq);
-        load_scales(a.k_sf, kbase + (tv + 1) * 128, min(128, a.Sk - (tv + 1) * 128), half, sfk);
-      }
+      uint32_t sfk[4] = {0u, 0u, 0u, 0u};
+      if (wsf) load_scales(a.k_sf, kbase + (tv + 1) * 128, min(128, a.Sk - (tv + 1) * 128), half, sfk);
       if (!warp_wait(&B.s_full[s], (t >> 1) & 1, ctl)) { ok = false; break; }
       tc_fence_after();
       const uint32_t pcol = tmem + lane_off + L::kColS0 + s * 128 + half * 64;   // this warp's S columns
@@ -422,22 +443,24 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       for (int k = 0; k < 32; ++k) pw[k] = pack_bf16x2(P[2 * k], P[2 * k + 1]);
 #pragma unroll
       for (int g = 0; g < 4; ++g) fake_nvfp4_16_pack_nonneg<false>(P + 16 * g, 1.0f, phw + 8 * g);
-      // P over columns [0,32) of this warp's S columns, P^ over [32,64)
+      // P over columns [0,32) of this warp's S columns, P^ over [32,64): the
+      // last 8 P^ columns (keys 48..63 of the half) are handed over separately
+      // because they hold the scale factors of S(t + 1) until it is complete
       tmem_st32(pcol, pw);
-      if (wsf) {
-        // P^ columns [32,40) hold the scale factors of S(t + 1): write them once it is complete
-        tmem_st16_nowait(pcol + 40, phw + 8);
-        tmem_st8_nowait(pcol + 56, phw + 24);
-        tmem_wait_st();
-        if (!warp_wait(&B.s_full[(t + 1) & 1], ((t + 1) >> 1) & 1, ctl)) { ok = false; break; }
-        tc_fence_after();
-        tmem_st8_nowait(pcol + 32, phw);
-        tmem_wait_st();
-      } else {
-        tmem_st32(pcol + 32, phw);
-      }
+      tmem_st16_nowait(pcol + 32, phw);
+      tmem_st8_nowait(pcol + 48, phw + 16);
+      if (!wsf) tmem_st8_nowait(pcol + 56, phw + 24);
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&B.p_ready[s]);
+      if (wsf) {
+        if (!warp_wait(&B.s_full[(t + 1) & 1], ((t + 1) >> 1) & 1, ctl)) { ok = false; break; }
+        tc_fence_after();
+        tmem_st8_nowait(pcol + 56, phw + 24);
+        tmem_wait_st();
+        tc_fence_before();
+      }
+      mbar_arrive(&B.p_late[s]);
     }
     // epilogue: O' and O rows, columns [half*D/2, +D/2)
     // (a one-shot barrier committed after the last O' and O MMAs)
