@@ -19,8 +19,8 @@
 //   S  = Q^_i K^T        (128 columns, lane = query row)
 //   dP = dO_i V^T        (128 columns)
 //   dV += P^T dO_i       (cols [256,256+D), lane = key)   A = P^ from smem (MN-major)
-//   dK += dS^T Q^_i      (cols [256+D,256+2D))            A = dS from smem (MN-major)
 //   dQ_i = dS K^         (over dP_i once it is read)      A = dS (K-major)
+//   dK += dS^T Q^_i      (cols [256+D,256+2D))            A = dS from smem (MN-major)
 // S, dP and dQ share two 128-column TMEM regions R0 = [0,128), R1 = [128,256).
 // Step `it` keeps dP and then dQ in R[(it+1)%2]; S of step it >= 1 is there
 // too (read before dP is written), S of step 0 is in R0. So dP of a step waits
@@ -262,10 +262,12 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
 
         if (!mbar_wait(&B.ds_ready, it & 1, ctl)) break;
         tc_fence_after();
-        mma_tn(L::kPS, s ? L::kQ1 : L::kQ0, L::kColDK, it > 0);
-        umma_commit(&B.q_empty[s]);
+        // dQ first, so that its drain (which frees the region S of step
+        // it + 2 goes to) starts one GEMM earlier
         mma_dq(dp_region(it));
         umma_commit(&B.dq_full);
+        mma_tn(L::kPS, s ? L::kQ1 : L::kQ0, L::kColDK, it > 0);
+        umma_commit(&B.q_empty[s]);
         umma_commit(&B.buf_free);
       }
       // Every MMA issued above completes before TMEM and smem are released.
