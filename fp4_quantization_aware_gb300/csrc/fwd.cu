@@ -30,10 +30,10 @@
 // in TMEM. For pass 1 and the first two pass-2 tiles they are in the O'
 // columns, which hold no accumulator yet: Q at O' + [0,8), K of tile t at
 // O' + 16 + 16 (t % 2) + [0,8). For a later pass-2 tile t + 1 they are in
-// columns 64h + [32,40) of S(t)'s buffer (K step h), written by the softmax
-// warps of half h as soon as they have read S(t); those warps write the first
-// 8 P^ columns of tile t there once S(t + 1) is complete. Shared memory:
-// V^ x3 96K, NVFP4 Q 8K, NVFP4 K x3 24K.
+// columns 64h + [56,64) of S(t)'s buffer (K step h), written by the softmax
+// warps of half h as soon as they have read S(t). The P^ of each key half's
+// last 16 keys, whose columns those are, goes through shared memory instead.
+// Shared memory: V^ x3 96K, NVFP4 Q 8K, NVFP4 K x3 24K, last-16-key P^ x2.
 // D = 64: S on BF16 MMAs from Q^, K^ in both passes. Shared memory: V^ x3,
 // Q^, K^ x3.
 #include "attn_common.cuh"
@@ -59,7 +59,11 @@ struct FwdLayout {
   // D = 128: NVFP4 Q, K (stage s at kK40 + s * kFp4Tile)
   static constexpr uint32_t kQ4 = kV0 + kStages * kTile;
   static constexpr uint32_t kK40 = kQ4 + kFp4Tile;
-  static constexpr uint32_t kML = kFp4 ? kK40 + kStages * kFp4Tile : kK0 + kStages * kTile;   // (m, l) of half 1, lse2
+  // D = 128: P^ of each key half's last 16 keys, per pass-2 tile parity: two
+  // 64-key K-major blocks (128-byte swizzle) of which only bytes 96..127 of
+  // each row are written and read
+  static constexpr uint32_t kPL0 = kK40 + kStages * kFp4Tile;
+  static constexpr uint32_t kML = kFp4 ? kPL0 + 2 * 2 * kBlockBytes : kK0 + kStages * kTile;   // (m, l) of half 1, lse2
   static constexpr uint32_t kBar = kML + 1536;
   static constexpr uint32_t kBytes = kBar + 256;
   static constexpr uint32_t kAlloc = kBytes + 1024;
@@ -73,6 +77,7 @@ struct FwdLayout {
   // key half's last 16 keys (read by the last O MMA of that half)
   static constexpr uint32_t kColSFQ2 = 56;
   static constexpr uint32_t kColSFK2 = 60;
+  static_assert(!kFp4 || kPL0 % 1024 == 0, "P^ blocks need 1024-byte alignment for the 128-byte swizzle");
   static_assert(kColSFQ2 % 4 == 0 && kColSFK2 == kColSFQ2 + 4 && kColSFK2 + 4 == 64,
                 "pass-2 scale factors: 4-column aligned, over the last 8 P^ columns of a key half");
 };
@@ -85,8 +90,7 @@ struct FwdBars {
   uint64_t v_empty[3];
   uint64_t s_full[2];
   uint64_t s_free[2];
-  uint64_t p_ready[2];   // per S buffer: P and P^ of a pass-2 tile are in TMEM, but for
-  uint64_t p_late[2];    // the P^ columns of each key half's last 16 keys
+  uint64_t p_ready[2];   // per S buffer: P and P^ of a pass-2 tile are in place
   uint64_t o_done;       // one phase: every O' and O MMA has completed
   uint64_t ml_ready;
   uint64_t lse_ready;
@@ -140,8 +144,6 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     for (int s = 0; s < 2; ++s) mbar_init(&B.s_full[s], 1), mbar_init(&B.s_free[s], 256);
     mbar_init(&B.p_ready[0], 256);
     mbar_init(&B.p_ready[1], 256);
-    mbar_init(&B.p_late[0], 256);
-    mbar_init(&B.p_late[1], 256);
     mbar_init(&B.o_done, 1);
     mbar_init(&B.ml_ready, 128);
     mbar_init(&B.lse_ready, 128);
@@ -274,24 +276,21 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
           const uint32_t vb = L::kV0 + sv * L::kTile;
           const uint32_t sc = L::kColS0 + (t & 1) * 128;
           mma_pv(sc, vb, L::kColOP, tv > 0);        // O' += P V^
-          // O += P^ V^: the k-steps of each key half's last 16 keys go last,
-          // once their P^ columns are written (they may have held the scale
-          // factors of the next S)
+          // O += P^ V^. D = 128: the P^ of each key half's last 16 keys comes
+          // from shared memory (its TMEM columns hold the next S's scale factors)
           {
             const uint64_t dv = sdesc_advance(mnmaj, vb);
+            const uint64_t dl = sdesc_advance(kmaj, L::kPL0 + (tv & 1) * 2 * kBlockBytes);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-              if ((kk & 3) == 3) continue;
-              const uint32_t ac = sc + 32 + (kk >> 2) * 64 + (kk & 3) * 8;
-              umma_bf16_tmem_a(tmem + L::kColO, tmem + ac, sdesc_advance(dv, kk * 2048), kIdO,
-                               (tv > 0 || kk > 0) ? 1u : 0u);
-            }
-            if (!mbar_wait(&B.p_late[t & 1], pr_use & 1, ctl)) break;
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 3; kk < 8; kk += 4) {
-              const uint32_t ac = sc + 32 + (kk >> 2) * 64 + (kk & 3) * 8;
-              umma_bf16_tmem_a(tmem + L::kColO, tmem + ac, sdesc_advance(dv, kk * 2048), kIdO, 1u);
+              const uint32_t acc = (tv > 0 || kk > 0) ? 1u : 0u;
+              if (L::kFp4 && (kk & 3) == 3) {
+                umma_bf16(tmem + L::kColO, sdesc_advance(dl, (kk >> 2) * kBlockBytes + 3 * 32),
+                          sdesc_advance(dv, kk * 2048), kIdO, acc);
+              } else {
+                const uint32_t ac = sc + 32 + (kk >> 2) * 64 + (kk & 3) * 8;
+                umma_bf16_tmem_a(tmem + L::kColO, tmem + ac, sdesc_advance(dv, kk * 2048), kIdO, acc);
+              }
             }
           }
           umma_commit(&B.v_empty[sv]);
@@ -443,24 +442,24 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       for (int k = 0; k < 32; ++k) pw[k] = pack_bf16x2(P[2 * k], P[2 * k + 1]);
 #pragma unroll
       for (int g = 0; g < 4; ++g) fake_nvfp4_16_pack_nonneg<false>(P + 16 * g, 1.0f, phw + 8 * g);
-      // P over columns [0,32) of this warp's S columns, P^ over [32,64): the
-      // last 8 P^ columns (keys 48..63 of the half) are handed over separately
-      // because they hold the scale factors of S(t + 1) until it is complete
+      // P over columns [0,32) of this warp's S columns, P^ over [32,64). D = 128:
+      // P^ of the half's last 16 keys goes to shared memory instead (bytes
+      // 96..127 of the row), as its columns may hold the scale factors of
+      // S(t + 1); the buffer's previous tile, t - 2, is complete since S(t) is.
       tmem_st32(pcol, pw);
-      tmem_st16_nowait(pcol + 32, phw);
-      tmem_st8_nowait(pcol + 48, phw + 16);
-      if (!wsf) tmem_st8_nowait(pcol + 56, phw + 24);
-      tmem_wait_st();
+      if constexpr (L::kFp4) {
+        tmem_st16_nowait(pcol + 32, phw);
+        tmem_st8_nowait(pcol + 48, phw + 16);
+        const uint32_t blk = sbase + L::kPL0 + (tv & 1) * 2 * kBlockBytes + half * kBlockBytes;
+        st_shared_v4(sw128_chunk(blk, r, 6), phw[24], phw[25], phw[26], phw[27]);
+        st_shared_v4(sw128_chunk(blk, r, 7), phw[28], phw[29], phw[30], phw[31]);
+        fence_proxy_async_smem();
+        tmem_wait_st();
+      } else {
+        tmem_st32(pcol + 32, phw);
+      }
       tc_fence_before();
       mbar_arrive(&B.p_ready[s]);
-      if (wsf) {
-        if (!warp_wait(&B.s_full[(t + 1) & 1], ((t + 1) >> 1) & 1, ctl)) { ok = false; break; }
-        tc_fence_after();
-        tmem_st8_nowait(pcol + 56, phw + 24);
-        tmem_wait_st();
-        tc_fence_before();
-      }
-      mbar_arrive(&B.p_late[s]);
     }
     // epilogue: O' and O rows, columns [half*D/2, +D/2)
     // (a one-shot barrier committed after the last O' and O MMAs)
