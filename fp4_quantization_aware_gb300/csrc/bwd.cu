@@ -28,9 +28,9 @@
 // goes into the region whose dQ was drained one step earlier: the dQ drain is
 // off the critical path.
 // Warp roles (14 warps):
-//   0-7  softmax: P = exp2(S*c - lse2), P^ = fake_nvfp4(P) -> smem, dS -> smem
+//   0-7  softmax: P = exp2(S*c - lse2), P^ = fake_nvfp4(P) -> smem, scale*dS -> smem
 //        (warp w reads TMEM lanes 32*(w%4).., columns [64*(w/4), +64) of a tile)
-//   8-11 dQ drain: TMEM -> scaled FP32 -> swizzled smem -> TMA reduce-add into
+//   8-11 dQ drain: TMEM -> FP32 swizzled smem -> TMA reduce-add into
 //        the workspace's FP32 dQ accumulator (one 32x32 box per warp and chunk)
 //   12   TMA producer (lane 0)
 //   13   MMA issuer (lane 0); the whole warp allocates and frees TMEM
@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         dlt_out = __ldg(a.delta + (size_t)bh * a.Sq + row);
       }
     };
-    const float2 c22 = make_float2(a.c2, a.c2);
+    const float2 c22 = make_float2(a.c2, a.c2), sc2 = make_float2(a.scale, a.scale);
     float lse_next, dlt_next;
     row_stats(0, lse_next, dlt_next);
     for (int it = 0; it < n_it; ++it) {
@@ -337,11 +337,13 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       {
         uint32_t v[64];
         tmem_ld64(tmem + lane_off + dp_region(it) + half * 64, v);
-        const float2 ndl = make_float2(-dlt, -dlt);
+        // dS carries the softmax scale of dQ and dK: scale * P (dP - delta)
+        // = P (scale dP - scale delta), one FMA and one multiply per pair
+        const float2 nsd = make_float2(-dlt * a.scale, -dlt * a.scale);
 #pragma unroll
         for (int k = 0; k < 64; k += 2) {
           const float2 d = fmul2(make_float2(P[k], P[k + 1]),
-                                 fadd2(make_float2(__uint_as_float(v[k]), __uint_as_float(v[k + 1])), ndl));
+                                 ffma2(make_float2(__uint_as_float(v[k]), __uint_as_float(v[k + 1])), sc2, nsd));
           ds[k / 2] = pack_bf16x2(d.x, d.y);
         }
       }
@@ -351,14 +353,14 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
       fence_proxy_async_smem();
       mbar_arrive(&B.ds_ready);
     }
-    // Epilogue: warps 0-3 own dK rows (scaled), warps 4-7 dV rows, one key row
+    // Epilogue: warps 0-3 own dK rows, warps 4-7 dV rows, one key row
     // per thread. A whole key tile stores BF16 rows. A split key tile adds its
     // FP32 partial rows into the tile's workspace slot; after both CTAs have
     // counted (device-scope fences around the count), the second one stores
     // the BF16 sums. Neither waits for the other.
     const int krow = j * 128 + r;
     const uint32_t col = half == 0 ? L::kColDK : L::kColDV;
-    const float mul = half == 0 ? a.scale : 1.0f;
+    const float mul = 1.0f;   // the softmax scale of dK is already in dS
     bf16* out = (half == 0 ? a.dk : a.dv) + ((size_t)bh * a.Sk + krow) * D;
     const bool have = ok && n_it > 0 && warp_wait(&B.buf_free, (n_it - 1) & 1, ctl);
     if (have) tc_fence_after();
@@ -430,10 +432,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
         const uint32_t st = stage0 + b * 4096;
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          st_shared_v4(sw128_chunk(st, lane, k), __float_as_uint(__uint_as_float(v[4 * k]) * a.scale),
-                       __float_as_uint(__uint_as_float(v[4 * k + 1]) * a.scale),
-                       __float_as_uint(__uint_as_float(v[4 * k + 2]) * a.scale),
-                       __float_as_uint(__uint_as_float(v[4 * k + 3]) * a.scale));
+          st_shared_v4(sw128_chunk(st, lane, k), v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
