@@ -54,6 +54,8 @@ SIGNATURES = {
     "attnqat_bwd_main": (_S, [_PP, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "attnqat_bwd_dq_convert": (_S, [_PP, _P, _P, ctypes.c_size_t, _P]),
     "attnqat_bwd_noalloc": (_S, [_PP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "attnqat_bwd_host_workspace_bytes": (ctypes.c_size_t, [_PP, ctypes.c_int]),
+    "attnqat_bwd_host": (_S, [_PP, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int, _P, ctypes.c_size_t, _P]),
     "attnqat_device_status": (_S, [ctypes.c_int]),
     "attnqat_selftest_wait_timeout": (_S, [ctypes.c_uint64, _P]),
     "attnqat_selftest_quotient": (_S, [_P, _P]),

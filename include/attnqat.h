@@ -111,6 +111,27 @@ attnqat_status attnqat_bwd(const attnqat_problem* p, const void* dout, const voi
                            const void* v, const void* o_hp, const float* lse, void* dq, void* dk, void* dv,
                            void* workspace, size_t workspace_bytes, void* stream);
 
+/* Backward with every input and output in host memory (page-locked, so that
+ * the copies overlap the kernels): the backward of the cuDNN page (Overview),
+ * computed by the same kernels as attnqat_bwd on groups of heads. The B*H
+ * heads are split into `chunks` contiguous groups (clamped to 1..B*H). While
+ * group c runs on `stream`, group c + 1 is copied in and group c - 1 out on
+ * two copy streams the library creates once per device. Arguments as for
+ * attnqat_bwd, with dout, q, k, v, o_hp, lse, dq, dk, dv host pointers in the
+ * same BHSD layouts. The device workspace of
+ * attnqat_bwd_host_workspace_bytes(p, chunks) bytes (256-byte aligned) holds
+ * two groups' inputs, outputs and backward workspace. The call returns once
+ * everything is enqueued; `stream` then waits for the last copy out, so
+ * synchronizing it makes dq, dk, dv readable. The host buffers must stay
+ * valid and unmodified until then. Results equal attnqat_bwd's up to the order
+ * of the FP32 additions of dQ and of split key tiles' partial dK, dV. Errors
+ * as attnqat_bwd; a failing CUDA call returns ATTNQAT_ERR_CUDA with part of
+ * the work enqueued. */
+size_t attnqat_bwd_host_workspace_bytes(const attnqat_problem* p, int chunks);
+attnqat_status attnqat_bwd_host(const attnqat_problem* p, const void* dout, const void* q, const void* k,
+                                const void* v, const void* o_hp, const float* lse, void* dq, void* dk, void* dv,
+                                int chunks, void* workspace, size_t workspace_bytes, void* stream);
+
 /* ---- the steps of attnqat_fwd / attnqat_bwd, for callers that time or
  * schedule them separately. Each takes the same workspace. ---- */
 

@@ -81,6 +81,25 @@ def test_workspace_sizes(clib):
     assert clib.attnqat_fwd_workspace_bytes(ctypes.byref(bad)) == 0
 
 
+def test_host_backward_workspace_sizes(clib):
+    """attnqat_bwd_host needs two head-group slots: each group's dO, Q, O',
+    K, V, LSE, dQ, dK, dV and its attnqat_bwd workspace (256-byte rounded)."""
+    p = attnqat.problem(1, 16, 4096, 4096, 128)
+    r = lambda x: (x + 255) // 256 * 256
+    g = attnqat.problem(1, 4, 4096, 4096, 128)          # 16 heads in 4 groups of 4
+    tile = 4 * 4096 * 128 * 2
+    slot = 8 * r(tile) + r(4 * 4096 * 4) + r(clib.attnqat_bwd_workspace_bytes(ctypes.byref(g)))
+    assert clib.attnqat_bwd_host_workspace_bytes(ctypes.byref(p), 4) == 2 * slot
+    # chunks are clamped to 1 .. B*H; unsupported problems give 0
+    one = attnqat.problem(1, 1, 4096, 4096, 128)
+    slot1 = 8 * r(tile // 4) + r(4096 * 4) + r(clib.attnqat_bwd_workspace_bytes(ctypes.byref(one)))
+    assert clib.attnqat_bwd_host_workspace_bytes(ctypes.byref(p), 100) == 2 * slot1
+    assert clib.attnqat_bwd_host_workspace_bytes(ctypes.byref(p), 0) == clib.attnqat_bwd_host_workspace_bytes(
+        ctypes.byref(p), 1)
+    bad = attnqat.problem(1, 1, 10, 10, 96)
+    assert clib.attnqat_bwd_host_workspace_bytes(ctypes.byref(bad), 2) == 0
+
+
 def test_errors_before_any_launch(clib):
     p = attnqat.problem(1, 1, 128, 128, 64)
     buf = ctypes.create_string_buffer(1 << 20)
