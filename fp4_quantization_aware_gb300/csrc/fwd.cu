@@ -16,12 +16,12 @@
 //
 // TMEM columns: S double-buffered [0,128) and [128,256); O' [256,256+D);
 // O [256+D,256+2D). In pass 2 the softmax warps write P and P^ (BF16 pairs)
-// back over the S tile they read: the warps of key half h (keys 64h..64h+63)
-// put P in columns 64h + [0,32) and P^ in 64h + [32,64) of that S buffer,
+// back over the S tile they read: the warps of key part p (keys 32p..32p+31)
+// put P in columns 32p + [0,16) and P^ in 32p + [16,32) of that S buffer,
 // columns only they read, and the O' and O MMAs take their A operand from
 // TMEM there. The next S goes into a buffer once the MMAs reading its P are
-// done (issue order). Warp roles (10 warps): 0-7 softmax (warp w: lanes
-// 32*(w%4).., key columns [64*(w/4), +64)); 8 TMA producer; 9 MMA issuer.
+// done (issue order). Warp roles (18 warps): 0-15 softmax (warp w: lanes
+// 32*(w%4).., key columns [32*(w/4), +32)); 16 TMA producer; 17 MMA issuer.
 // K^ and V^ tiles are triple-buffered in shared memory.
 //
 // D = 128: both passes compute S on the block-scaled NVFP4 tensor-core MMA
@@ -31,8 +31,9 @@
 // columns, which hold no accumulator yet: Q at O' + [0,8), K of tile t at
 // O' + 16 + 16 (t % 2) + [0,8). For a later pass-2 tile t + 1 they are in
 // columns 64h + [56,64) of S(t)'s buffer (K step h), written by the softmax
-// warps of half h as soon as they have read S(t). The P^ of each key half's
-// last 16 keys, whose columns those are, goes through shared memory instead.
+// warps of key part 2h + 1 as soon as they have read S(t). The P^ of each key
+// half's last 16 keys, whose columns those are, goes through shared memory
+// instead.
 // Shared memory: V^ x3 96K, NVFP4 Q 8K, NVFP4 K x3 24K, last-16-key P^ x2.
 // D = 64: S on BF16 MMAs from Q^, K^ in both passes. Shared memory: V^ x3,
 // Q^, K^ x3.
@@ -42,9 +43,10 @@
 namespace attnqat {
 namespace {
 
-constexpr int kThreadsFwd = 10 * 32;
-constexpr int kWarpTmaF = 8;
-constexpr int kWarpMmaF = 9;
+constexpr int kSoftWarpsF = 16;                 // 4 per lane quarter, 32 keys of a tile each
+constexpr int kThreadsFwd = (kSoftWarpsF + 2) * 32;
+constexpr int kWarpTmaF = kSoftWarpsF;
+constexpr int kWarpMmaF = kSoftWarpsF + 1;
 
 template <int D>
 struct FwdLayout {
@@ -63,8 +65,9 @@ struct FwdLayout {
   // 64-key K-major blocks (128-byte swizzle) of which only bytes 96..127 of
   // each row are written and read
   static constexpr uint32_t kPL0 = kK40 + kStages * kFp4Tile;
-  static constexpr uint32_t kML = kFp4 ? kPL0 + 2 * 2 * kBlockBytes : kK0 + kStages * kTile;   // (m, l) of half 1, lse2
-  static constexpr uint32_t kBar = kML + 1536;
+  // 128 rows x (m, l) of key parts 1..3, then 128 lse2
+  static constexpr uint32_t kML = kFp4 ? kPL0 + 2 * 2 * kBlockBytes : kK0 + kStages * kTile;
+  static constexpr uint32_t kBar = kML + 3 * 128 * 8 + 128 * 4;
   static constexpr uint32_t kBytes = kBar + 256;
   static constexpr uint32_t kAlloc = kBytes + 1024;
   static constexpr uint32_t kColS0 = 0;
@@ -141,14 +144,14 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       mbar_init(&B.k_full[s], 1), mbar_init(&B.k_empty[s], 1);
       mbar_init(&B.v_full[s], 1), mbar_init(&B.v_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) mbar_init(&B.s_full[s], 1), mbar_init(&B.s_free[s], 256);
-    mbar_init(&B.p_ready[0], 256);
-    mbar_init(&B.p_ready[1], 256);
+    for (int s = 0; s < 2; ++s) mbar_init(&B.s_full[s], 1), mbar_init(&B.s_free[s], kSoftWarpsF * 32);
+    mbar_init(&B.p_ready[0], kSoftWarpsF * 32);
+    mbar_init(&B.p_ready[1], kSoftWarpsF * 32);
     mbar_init(&B.o_done, 1);
-    mbar_init(&B.ml_ready, 128);
-    mbar_init(&B.lse_ready, 128);
+    mbar_init(&B.ml_ready, 3 * 128);   // key parts 1..3
+    mbar_init(&B.lse_ready, 128);      // key part 0
     mbar_init(&B.drain, 1);
-    mbar_init(&B.sf_init, 256);
+    mbar_init(&B.sf_init, 2 * 128);    // key parts 1 and 3
     fence_mbar_init();
   }
   if (warp == kWarpMmaF) {
@@ -252,13 +255,13 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         return true;
       };
       // O (+)= A[128 q x 128 keys] V^[128 keys x D]: A from TMEM at `a_col`
-      // (keys 0..63 in columns a_col + [0,32), keys 64..127 in a_col + 64 + [0,32)),
-      // V^ MN-major in shared memory.
+      // (keys 32p .. 32p + 31 in columns a_col + 32p + [0,16)), V^ MN-major in
+      // shared memory.
       auto mma_pv = [&](uint32_t a_col, uint32_t v_off, uint32_t col, bool acc) {
         const uint64_t dv = sdesc_advance(mnmaj, v_off);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t ac = a_col + (kk >> 2) * 64 + (kk & 3) * 8;
+          const uint32_t ac = a_col + (kk >> 1) * 32 + (kk & 1) * 8;
           umma_bf16_tmem_a(tmem + col, tmem + ac, sdesc_advance(dv, kk * 2048), kIdO, (acc || kk > 0) ? 1u : 0u);
         }
       };
@@ -288,7 +291,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
                 umma_bf16(tmem + L::kColO, sdesc_advance(dl, (kk >> 2) * kBlockBytes + 3 * 32),
                           sdesc_advance(dv, kk * 2048), kIdO, acc);
               } else {
-                const uint32_t ac = sc + 32 + (kk >> 2) * 64 + (kk & 3) * 8;
+                const uint32_t ac = sc + 16 + (kk >> 1) * 32 + (kk & 1) * 8;
                 umma_bf16_tmem_a(tmem + L::kColO, tmem + ac, sdesc_advance(dv, kk * 2048), kIdO, acc);
               }
             }
@@ -301,70 +304,77 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       mbar_wait_drain(&B.drain, 0, ctl);
     }
   } else {
-    // ------------------------------------------------------------ softmax (warps 0-7)
-    const uint32_t quarter = warp & 3, half = warp >> 2;
+    // ------------------------------------------------------------ softmax (warps 0-15)
+    // Warp w owns lane quarter w % 4 (32 query rows) and key part w / 4 (keys
+    // 32 p .. 32 p + 31 of every tile, S columns [32 p, 32 p + 32)). In pass 2
+    // it writes P over columns 32 p + [0,16) and P^ over 32 p + [16,32). Parts
+    // 1 and 3 also write the scale factors (K step p / 2); in pass 2 those go
+    // over their P^ columns 32 p + [24,32), whose P^ goes to shared memory.
+    const uint32_t quarter = warp & 3, part = warp >> 2;
+    const bool sf_writer = (part & 1u) != 0;
+    const int ks = static_cast<int>(part >> 1);
     const uint32_t r = quarter * 32 + lane;
     const uint32_t lane_off = (quarter * 32u) << 16;
     const int qrow = i * 128 + r;
     const int kend = a.causal ? min(a.Sk, qrow + 1) : a.Sk;
     const int64_t kbase = static_cast<int64_t>(bh) * a.Sk;
     bool ok = true;
-    if (L::kFp4) {   // pass-1 scale factors: this warp writes K step `half` of each block
+    if (L::kFp4 && sf_writer) {   // pass-1 scale factors of K step ks
       uint32_t w[4];
-      load_scales(a.q_sf, static_cast<int64_t>(bh) * a.Sq + i * 128, min(128, a.Sq - i * 128), half, w);
-      tmem_st4(tmem + lane_off + L::kColSFQ + 4 * half, w);
-      load_scales(a.k_sf, kbase, min(128, a.Sk), half, w);
-      tmem_st4(tmem + lane_off + L::kColSFK0 + 4 * half, w);
+      load_scales(a.q_sf, static_cast<int64_t>(bh) * a.Sq + i * 128, min(128, a.Sq - i * 128), ks, w);
+      tmem_st4(tmem + lane_off + L::kColSFQ + 4 * ks, w);
+      load_scales(a.k_sf, kbase, min(128, a.Sk), ks, w);
+      tmem_st4(tmem + lane_off + L::kColSFK0 + 4 * ks, w);
       const int kt1 = nk > 1 ? 1 : 0;   // tile 1 is pass 2's first when nk = 1
-      load_scales(a.k_sf, kbase + kt1 * 128, min(128, a.Sk - kt1 * 128), half, w);
-      tmem_st4(tmem + lane_off + L::kColSFK1 + 4 * half, w);
+      load_scales(a.k_sf, kbase + kt1 * 128, min(128, a.Sk - kt1 * 128), ks, w);
+      tmem_st4(tmem + lane_off + L::kColSFK1 + 4 * ks, w);
       tc_fence_before();
       mbar_arrive(&B.sf_init);
     }
 
-    // pass 1: running max and sum of exp2(S * c2) over this thread's key columns
+    // pass 1: running max and sum of exp2(S * c2) over this thread's 32 key columns
     const float2 c22 = make_float2(a.c2, a.c2);
     float m = -INFINITY, l = 0.0f;
     for (int t = 0; t < nk; ++t) {
       const int s = t & 1;
-      const int valid = kend - (t * 128 + static_cast<int>(half) * 64);
+      const int valid = kend - (t * 128 + static_cast<int>(part) * 32);
       // K scales of tile t + 2 (up to pass 2's second tile, key tile 1)
-      const bool more = L::kFp4 && t + 2 < nt;
+      const bool more = L::kFp4 && sf_writer && t + 2 < nt;
       const int kt2 = t + 2 < nk ? t + 2 : t + 2 - nk;
       uint32_t sfw[4] = {0u, 0u, 0u, 0u};
-      if (more) load_scales(a.k_sf, kbase + kt2 * 128, min(128, a.Sk - kt2 * 128), half, sfw);
+      if (more) load_scales(a.k_sf, kbase + kt2 * 128, min(128, a.Sk - kt2 * 128), ks, sfw);
       if (!warp_wait(&B.s_full[s], (t >> 1) & 1, ctl)) { ok = false; break; }
       tc_fence_after();
-      uint32_t v[64];
-      tmem_ld64(tmem + lane_off + L::kColS0 + s * 128 + half * 64, v);
+      uint32_t v[32];
+      tmem_ld32(tmem + lane_off + L::kColS0 + s * 128 + part * 32, v);
       // tile t + 2's K scales into the slot S(t) used (S(t) is complete);
       // releasing S(t) below also certifies them to the MMA issuer
-      if (more) tmem_st4(tmem + lane_off + (s ? L::kColSFK1 : L::kColSFK0) + 4 * half, sfw);
+      if (more) tmem_st4(tmem + lane_off + (s ? L::kColSFK1 : L::kColSFK0) + 4 * ks, sfw);
       tc_fence_before();
       mbar_arrive(&B.s_free[s]);
-      if (valid < 64) {   // masked keys: -inf
+      if (valid < 32) {   // masked keys: -inf
 #pragma unroll
-        for (int k = 0; k < 64; ++k)
+        for (int k = 0; k < 32; ++k)
           if (k >= valid) v[k] = 0xFF800000u;
       }
-      // Row max of the raw S (four chains of 3-input max); c2 > 0 and rounding
+      // Row max of the raw S (two chains of 3-input max); c2 > 0 and rounding
       // is monotonic, so max(S) * c2 is the max of the scaled logits.
-      float mq[4];
+      float mq[2];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < 2; ++u) {
         float acc = fmaxf(__uint_as_float(v[16 * u]), __uint_as_float(v[16 * u + 1]));
 #pragma unroll
         for (int k = 2; k < 16; k += 2) acc = fmax3(acc, __uint_as_float(v[16 * u + k]), __uint_as_float(v[16 * u + k + 1]));
         mq[u] = acc;
       }
-      const float mx = fmaxf(m, fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * a.c2);
+      const float mx = fmaxf(m, fmaxf(mq[0], mq[1]) * a.c2);
       if (mx == -INFINITY) continue;
       // sum of exp2(S * c2 - mx), arguments and partial sums as packed pairs
       const float2 nm = make_float2(-mx, -mx);
       float2 sc[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
                       make_float2(0.0f, 0.0f)};
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
+      for (int k = 0; k < 16; ++k) {
         const float2 e = ffma2(make_float2(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1])), c22, nm);
         sc[k & 3] = fadd2(sc[k & 3], make_float2(ex2(e.x), ex2(e.y)));
       }
@@ -372,13 +382,13 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       l = l * ex2(m - mx) + (st.x + st.y);
       m = mx;
     }
-    // Combine the two column halves of each row: half 1 hands (m, l) to half
+    // Combine the four key parts of each row: parts 1..3 hand (m, l) to part
     // 0, which forms lse2 = log2 sum 2^(S*c2), stores LSE and hands lse2 back.
     float lse2 = 0.0f;
-    float* lse_s = ml + 256;
-    if (ok && half == 1) {
-      ml[r * 2] = m;
-      ml[r * 2 + 1] = l;
+    float* lse_s = ml + 3 * 256;
+    if (ok && part != 0) {
+      ml[(part - 1) * 256 + r * 2] = m;
+      ml[(part - 1) * 256 + r * 2 + 1] = l;
       mbar_arrive(&B.ml_ready);
       if (warp_wait(&B.lse_ready, 0, ctl))
         lse2 = lse_s[r];
@@ -386,9 +396,12 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         ok = false;
     } else if (ok) {
       if (warp_wait(&B.ml_ready, 0, ctl)) {
-        const float m1 = ml[r * 2], l1 = ml[r * 2 + 1];
-        const float M = fmaxf(m, m1);
-        const float Lsum = (m == -INFINITY ? 0.0f : l * ex2(m - M)) + (m1 == -INFINITY ? 0.0f : l1 * ex2(m1 - M));
+        float mp[4] = {m, ml[r * 2], ml[256 + r * 2], ml[512 + r * 2]};
+        float lp[4] = {l, ml[r * 2 + 1], ml[256 + r * 2 + 1], ml[512 + r * 2 + 1]};
+        const float M = fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3]));
+        float Lsum = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) Lsum += mp[q] == -INFINITY ? 0.0f : lp[q] * ex2(mp[q] - M);
         lse2 = M + lg2(Lsum);
         lse_s[r] = lse2;
         mbar_arrive(&B.lse_ready);
@@ -399,81 +412,86 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     }
 
     // pass 2: P = exp2(S * c2 - lse2), P^ = fake_nvfp4(P); hand both to the MMA warp
-    uint32_t sfq[4] = {0u, 0u, 0u, 0u};   // D = 128: this half's K step of the Q scale factors
-    if (L::kFp4) load_scales(a.q_sf, static_cast<int64_t>(bh) * a.Sq + i * 128, min(128, a.Sq - i * 128), half, sfq);
+    uint32_t sfq[4] = {0u, 0u, 0u, 0u};   // D = 128: K step ks of the Q scale factors (parts 1, 3)
+    if (L::kFp4 && sf_writer)
+      load_scales(a.q_sf, static_cast<int64_t>(bh) * a.Sq + i * 128, min(128, a.Sq - i * 128), ks, sfq);
     for (int t = nk; ok && t < nt; ++t) {
       const int s = t & 1, tv = t - nk;
-      const int valid = kend - (tv * 128 + static_cast<int>(half) * 64);
-      // D = 128: this warp puts the scale factors of S(t + 1) (pass-2 tiles
-      // from the third on; K step `half`) into S(t)'s buffer, where its P^
-      // columns [32,40) go later
-      const bool wsf = L::kFp4 && tv >= 1 && t + 1 < nt;
+      const int valid = kend - (tv * 128 + static_cast<int>(part) * 32);
+      // D = 128: parts 1 and 3 put the scale factors of S(t + 1) (pass-2
+      // tiles from the third on; K step ks) into S(t)'s buffer, over the P^
+      // columns of the key half's last 16 keys
+      const bool wsf = L::kFp4 && sf_writer && tv >= 1 && t + 1 < nt;
       uint32_t sfk[4] = {0u, 0u, 0u, 0u};
-      if (wsf) load_scales(a.k_sf, kbase + (tv + 1) * 128, min(128, a.Sk - (tv + 1) * 128), half, sfk);
+      if (wsf) load_scales(a.k_sf, kbase + (tv + 1) * 128, min(128, a.Sk - (tv + 1) * 128), ks, sfk);
       if (!warp_wait(&B.s_full[s], (t >> 1) & 1, ctl)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t pcol = tmem + lane_off + L::kColS0 + s * 128 + half * 64;   // this warp's S columns
-      float P[64];
+      const uint32_t pcol = tmem + lane_off + L::kColS0 + s * 128 + part * 32;   // this warp's S columns
+      float P[32];
       {
-        uint32_t v[64];
-        tmem_ld64(pcol, v);
+        uint32_t v[32];
+        tmem_ld32(pcol, v);
         if constexpr (L::kFp4) {   // S(t) is read: scale factors of S(t + 1), then release it
           if (wsf) {
-            tmem_st4(pcol + L::kColSFQ2, sfq);
-            tmem_st4(pcol + L::kColSFK2, sfk);
+            tmem_st4(pcol + 24, sfq);
+            tmem_st4(pcol + 28, sfk);
           }
           tc_fence_before();
           mbar_arrive(&B.s_free[s]);
         }
         const float2 nl = make_float2(-lse2, -lse2);
 #pragma unroll
-        for (int k = 0; k < 64; k += 2) {
+        for (int k = 0; k < 32; k += 2) {
           const float2 e = ffma2(make_float2(__uint_as_float(v[k]), __uint_as_float(v[k + 1])), c22, nl);
           P[k] = ex2(e.x), P[k + 1] = ex2(e.y);
         }
       }
-      if (valid < 64) {   // masked keys: P = 0
+      if (valid < 32) {   // masked keys: P = 0
 #pragma unroll
-        for (int k = 0; k < 64; ++k)
+        for (int k = 0; k < 32; ++k)
           if (k >= valid) P[k] = 0.0f;
       }
-      uint32_t pw[32], phw[32];
+      uint32_t pw[16], phw[16];
 #pragma unroll
-      for (int k = 0; k < 32; ++k) pw[k] = pack_bf16x2(P[2 * k], P[2 * k + 1]);
+      for (int k = 0; k < 16; ++k) pw[k] = pack_bf16x2(P[2 * k], P[2 * k + 1]);
 #pragma unroll
-      for (int g = 0; g < 4; ++g) fake_nvfp4_16_pack_nonneg<false>(P + 16 * g, 1.0f, phw + 8 * g);
-      // P over columns [0,32) of this warp's S columns, P^ over [32,64). D = 128:
-      // P^ of the half's last 16 keys goes to shared memory instead (bytes
-      // 96..127 of the row), as its columns may hold the scale factors of
-      // S(t + 1); the buffer's previous tile, t - 2, is complete since S(t) is.
-      tmem_st32(pcol, pw);
-      if constexpr (L::kFp4) {
-        tmem_st16_nowait(pcol + 32, phw);
-        tmem_st8_nowait(pcol + 48, phw + 16);
-        const uint32_t blk = sbase + L::kPL0 + (tv & 1) * 2 * kBlockBytes + half * kBlockBytes;
-        st_shared_v4(sw128_chunk(blk, r, 6), phw[24], phw[25], phw[26], phw[27]);
-        st_shared_v4(sw128_chunk(blk, r, 7), phw[28], phw[29], phw[30], phw[31]);
+      for (int g = 0; g < 2; ++g) fake_nvfp4_16_pack_nonneg<false>(P + 16 * g, 1.0f, phw + 8 * g);
+      // P over columns [0,16) of this warp's S columns, P^ over [16,32). D = 128:
+      // parts 1 and 3 send the P^ of the key half's last 16 keys to shared
+      // memory instead (bytes 96..127 of the row of the half's 64-key block),
+      // as its columns may hold the scale factors of S(t + 1); the buffer's
+      // previous tile, t - 2, is complete since S(t) is.
+      tmem_st16_nowait(pcol, pw);
+      if (L::kFp4 && sf_writer) {
+        tmem_st8_nowait(pcol + 16, phw);
+        const uint32_t blk = sbase + L::kPL0 + (tv & 1) * 2 * kBlockBytes + ks * kBlockBytes;
+        st_shared_v4(sw128_chunk(blk, r, 6), phw[8], phw[9], phw[10], phw[11]);
+        st_shared_v4(sw128_chunk(blk, r, 7), phw[12], phw[13], phw[14], phw[15]);
         fence_proxy_async_smem();
-        tmem_wait_st();
       } else {
-        tmem_st32(pcol + 32, phw);
+        tmem_st16_nowait(pcol + 16, phw);
       }
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&B.p_ready[s]);
     }
-    // epilogue: O' and O rows, columns [half*D/2, +D/2)
-    // (a one-shot barrier committed after the last O' and O MMAs)
+    // epilogue: O' and O rows (a one-shot barrier committed after the last O'
+    // and O MMAs). D = 128: part p stores columns [32 p, 32 p + 32) of both;
+    // D = 64: parts 0, 1 store O' columns [32 (p % 2), +32), parts 2, 3 O's.
     if (ok && warp_wait(&B.o_done, 0, ctl)) {
       tc_fence_after();
       const size_t row = (size_t)bh * a.Sq + qrow;
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        const uint32_t col = half * (D / 2) + c * 32;
-        uint32_t v[32];
+      uint32_t v[32];
+      if constexpr (D == 128) {
+        const uint32_t col = part * 32;
         tmem_ld32(tmem + lane_off + L::kColOP + col, v);
         if (qrow < a.Sq) store_row32_bf16(a.o_hp + row * D + col, v, 1.0f);
         tmem_ld32(tmem + lane_off + L::kColO + col, v);
         if (qrow < a.Sq) store_row32_bf16(a.o + row * D + col, v, 1.0f);
+      } else {
+        const uint32_t col = (part & 1) * 32;
+        tmem_ld32(tmem + lane_off + (part < 2 ? L::kColOP : L::kColO) + col, v);
+        if (qrow < a.Sq) store_row32_bf16((part < 2 ? a.o_hp : a.o) + row * D + col, v, 1.0f);
       }
     }
   }
