@@ -43,16 +43,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return ok != 0;
 }
 
-// The same with cluster-scope acquire, for barriers that a peer CTA of the
-// cluster arrives on.
-__device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity, const WaitCtl& c) {
-  uint32_t ok = 0;
-  if (lane_id() == 0) ok = mbar_wait_cluster(bar, parity, c) ? 1u : 0u;
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  if (ok && lane_id() != 0) (void)mbar_try_wait_cluster(bar, parity);   // each lane's own acquire
-  __syncwarp();
-  return ok != 0;
-}
 
 // Store one thread's 64 packed BF16 values (32 words) as row `row` of the
 // 64-column block at `block_base`.
