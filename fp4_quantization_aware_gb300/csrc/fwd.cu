@@ -335,14 +335,19 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     // pass 1: running max and sum of exp2(S * c2) over this thread's 32 key columns
     const float2 c22 = make_float2(a.c2, a.c2);
     float m = -INFINITY, l = 0.0f;
+    // K scales written at tile t (those of tile t + 2, up to pass 2's second
+    // tile) are loaded one tile ahead, so their latency is off the hand-off
+    auto kt_of = [&](int u) { return u < nk ? u : u - nk; };
+    uint32_t sfw[4] = {0u, 0u, 0u, 0u}, sfw_next[4] = {0u, 0u, 0u, 0u};
+    if (L::kFp4 && sf_writer && 2 < nt)
+      load_scales(a.k_sf, kbase + kt_of(2) * 128, min(128, a.Sk - kt_of(2) * 128), ks, sfw);
     for (int t = 0; t < nk; ++t) {
       const int s = t & 1;
       const int valid = kend - (t * 128 + static_cast<int>(part) * 32);
       // K scales of tile t + 2 (up to pass 2's second tile, key tile 1)
       const bool more = L::kFp4 && sf_writer && t + 2 < nt;
-      const int kt2 = t + 2 < nk ? t + 2 : t + 2 - nk;
-      uint32_t sfw[4] = {0u, 0u, 0u, 0u};
-      if (more) load_scales(a.k_sf, kbase + kt2 * 128, min(128, a.Sk - kt2 * 128), ks, sfw);
+      if (L::kFp4 && sf_writer && t + 3 < nt && t + 1 < nk)
+        load_scales(a.k_sf, kbase + kt_of(t + 3) * 128, min(128, a.Sk - kt_of(t + 3) * 128), ks, sfw_next);
       if (!warp_wait(&B.s_full[s], (t >> 1) & 1, ctl)) { ok = false; break; }
       tc_fence_after();
       uint32_t v[32];
@@ -352,6 +357,8 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       if (more) tmem_st4(tmem + lane_off + (s ? L::kColSFK1 : L::kColSFK0) + 4 * ks, sfw);
       tc_fence_before();
       mbar_arrive(&B.s_free[s]);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) sfw[q] = sfw_next[q];
       if (valid < 32) {   // masked keys: -inf
 #pragma unroll
         for (int k = 0; k < 32; ++k)
@@ -415,6 +422,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     uint32_t sfq[4] = {0u, 0u, 0u, 0u};   // D = 128: K step ks of the Q scale factors (parts 1, 3)
     if (L::kFp4 && sf_writer)
       load_scales(a.q_sf, static_cast<int64_t>(bh) * a.Sq + i * 128, min(128, a.Sq - i * 128), ks, sfq);
+    uint32_t sfk[4] = {0u, 0u, 0u, 0u};
     for (int t = nk; ok && t < nt; ++t) {
       const int s = t & 1, tv = t - nk;
       const int valid = kend - (tv * 128 + static_cast<int>(part) * 32);
@@ -422,8 +430,10 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       // tiles from the third on; K step ks) into S(t)'s buffer, over the P^
       // columns of the key half's last 16 keys
       const bool wsf = L::kFp4 && sf_writer && tv >= 1 && t + 1 < nt;
-      uint32_t sfk[4] = {0u, 0u, 0u, 0u};
-      if (wsf) load_scales(a.k_sf, kbase + (tv + 1) * 128, min(128, a.Sk - (tv + 1) * 128), ks, sfk);
+      // sfk holds key tile tv + 1's scales (loaded one tile ahead); fetch tv + 2's
+      uint32_t sfk_next[4] = {0u, 0u, 0u, 0u};
+      if (L::kFp4 && sf_writer && tv + 2 < nk)
+        load_scales(a.k_sf, kbase + (tv + 2) * 128, min(128, a.Sk - (tv + 2) * 128), ks, sfk_next);
       if (!warp_wait(&B.s_full[s], (t >> 1) & 1, ctl)) { ok = false; break; }
       tc_fence_after();
       const uint32_t pcol = tmem + lane_off + L::kColS0 + s * 128 + part * 32;   // this warp's S columns
@@ -439,6 +449,8 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
           tc_fence_before();
           mbar_arrive(&B.s_free[s]);
         }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) sfk[q] = sfk_next[q];
         const float2 nl = make_float2(-lse2, -lse2);
 #pragma unroll
         for (int k = 0; k < 32; k += 2) {
