@@ -37,7 +37,7 @@ size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsLayout {
   size_t qh, kh, vh, delta, dq_acc, split, split_slots, q4, qsf, k4, ksf, total;
-  bool packed;   // forward with D = 128: NVFP4 Q, K for the first pass
+  bool packed;   // D = 128: NVFP4 Q^, K^ and their scales for the S MMAs
 };
 
 Problem to_problem(const attnqat_problem& p) {
@@ -59,7 +59,8 @@ WsLayout layout(const attnqat_problem& p, bool bwd) {
     w.split_slots = static_cast<size_t>(tiles < kMaxSplitTiles ? tiles : kMaxSplitTiles);
     w.split = off,
     off += round256((split_cnt_words() + w.split_slots * split_slot_floats(to_problem(p))) * 4);
-  } else if (p.D == 128) {
+  }
+  if (p.D == 128) {   // NVFP4 Q^, K^ for the S MMAs (forward passes, backward recompute)
     w.packed = true;
     w.q4 = off, off += round256(bh * p.Sq * 64);
     w.qsf = off, off += round256(bh * p.Sq * 8);
@@ -320,7 +321,9 @@ attnqat_status attnqat_bwd_preprocess(const attnqat_problem* p, const void* dout
                            at<float>(ws, w.split),
                            split_cnt_words() + bwd_split_plan(to_problem(*p), device_sm_count()).n_split *
                                                    split_slot_floats(to_problem(*p)),
-                           nullptr, nullptr, nullptr, nullptr, static_cast<cudaStream_t>(stream)),
+                           w.packed ? at<uint8_t>(ws, w.q4) : nullptr, w.packed ? at<uint8_t>(ws, w.qsf) : nullptr,
+                           w.packed ? at<uint8_t>(ws, w.k4) : nullptr, w.packed ? at<uint8_t>(ws, w.ksf) : nullptr,
+                           static_cast<cudaStream_t>(stream)),
                "bwd_preprocess");
   return ATTNQAT_OK;
 }
@@ -337,7 +340,9 @@ attnqat_status attnqat_bwd_main(const attnqat_problem* p, const void* dout, cons
   ATTNQAT_CUDA(launch_bwd(to_problem(*p), at<bf16>(ws, w.qh), at<bf16>(ws, w.kh), at<bf16>(ws, w.vh),
                           static_cast<const bf16*>(dout), lse, at<float>(ws, w.delta), at<float>(ws, w.dq_acc),
                           static_cast<bf16*>(dk), static_cast<bf16*>(dv), at<float>(ws, w.split) + split_cnt_words(),
-                          at<uint32_t>(ws, w.split), err, static_cast<cudaStream_t>(stream)),
+                          at<uint32_t>(ws, w.split), w.packed ? at<uint8_t>(ws, w.q4) : nullptr,
+                          w.packed ? at<uint8_t>(ws, w.qsf) : nullptr, w.packed ? at<uint8_t>(ws, w.k4) : nullptr,
+                          w.packed ? at<uint8_t>(ws, w.ksf) : nullptr, err, static_cast<cudaStream_t>(stream)),
                "bwd_main");
   return ATTNQAT_OK;
 }

@@ -43,6 +43,24 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return ok != 0;
 }
 
+// Early, non-blocking poll of a barrier phase by lane 0 (1 if complete). Its
+// verdict is consumed by warp_wait_polled later, so the poll's latency (long
+// while the tensor core streams operands from shared memory) overlaps the
+// work issued in between.
+__device__ __forceinline__ uint32_t warp_poll(uint64_t* bar, uint32_t parity) {
+  return lane_id() == 0 && mbar_try_wait(bar, parity) ? 1u : 0u;
+}
+
+// warp_wait that lane 0 skips when its earlier warp_poll saw the phase done.
+__device__ __forceinline__ bool warp_wait_polled(uint32_t polled, uint64_t* bar, uint32_t parity,
+                                                 const WaitCtl& c) {
+  uint32_t ok = polled;
+  if (lane_id() == 0 && ok == 0u) ok = mbar_wait(bar, parity, c) ? 1u : 0u;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+
 
 // Store one thread's 64 packed BF16 values (32 words) as row `row` of the
 // 64-column block at `block_base`.

@@ -68,7 +68,8 @@ cudaError_t launch_fwd_r2(const Problem& p, const bf16* qh, const bf16* kh, cons
 
 cudaError_t launch_bwd(const Problem& p, const bf16* qh, const bf16* kh, const bf16* vh, const bf16* dout,
                        const float* lse, const float* delta, float* dq_acc, bf16* dk, bf16* dv, float* split_acc,
-                       uint32_t* split_cnt, uint32_t* err, cudaStream_t st);
+                       uint32_t* split_cnt, const uint8_t* q4, const uint8_t* qsf, const uint8_t* k4,
+                       const uint8_t* ksf, uint32_t* err, cudaStream_t st);
 
 // Inference forward: O = softmax(scale * Q K^T) V with packed NVFP4 Q and K
 // ((B*H, S, 64) bytes of E2M1 pairs, (B*H, S, 8) E4M3 scales) and BF16 V;

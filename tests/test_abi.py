@@ -68,10 +68,12 @@ def test_workspace_sizes(clib):
     # Q^, K^, V^ (BF16) and, at D = 128, NVFP4 Q and K (E2M1 pairs + E4M3 scales)
     assert fwd == 3 * bh * 4096 * 128 * 2 + 2 * (bh * 4096 * 64 + bh * 4096 * 8)
     base = 3 * bh * 4096 * 128 * 2
-    # + delta, the FP32 dQ accumulator, and the split-tile area: 128 counter
-    # words and FP32 [dK, dV] slots for min(key tiles, 96) tiles
+    # + delta, the FP32 dQ accumulator, the split-tile area (128 counter words
+    # and FP32 [dK, dV] slots for min(key tiles, 96) tiles) and, at D = 128,
+    # the NVFP4 Q and K of the backward's S recompute
     split = 128 * 4 + min(bh * 4096 // 128, 96) * 2 * 128 * 128 * 4
-    assert bwd == base + bh * 4096 * 4 + bh * 4096 * 128 * 4 + split
+    packed = 2 * (bh * 4096 * 64 + bh * 4096 * 8)
+    assert bwd == base + bh * 4096 * 4 + bh * 4096 * 128 * 4 + split + packed
     small = attnqat.problem(1, 1, 100, 300, 64)      # 3 key tiles of 64-wide rows
     assert clib.attnqat_bwd_workspace_bytes(ctypes.byref(small)) == (
         256 * ((100 * 64 * 2 + 255) // 256) + 2 * 256 * ((300 * 64 * 2 + 255) // 256)
