@@ -506,7 +506,7 @@ static_assert(BwdFp4Layout::kAlloc <= 232448, "shared memory of the D = 128 back
 
 struct BwdFp4Bars {
   uint64_t kv_full, q_full, q_empty, q4_full, q4_empty, do_full, do_empty;
-  uint64_t s_full, s_free, dp_full, p_ready, p_free, ds_ready, ds_free, dq_full, dq_free, sf_init, drain;
+  uint64_t s_full, s_free, dp_full, p_ready, p_free, ds_ready, ds_free, dq_full, dq_free, sf_init, sf_ready, drain;
   uint32_t tmem_base;
   uint32_t abort_flag;
   uint32_t split_order;
@@ -548,6 +548,7 @@ __global__ void __maxnreg__(128)
     mbar_init(&B.s_full, 1), mbar_init(&B.dp_full, 1), mbar_init(&B.p_free, 1), mbar_init(&B.ds_free, 1);
     mbar_init(&B.dq_full, 1), mbar_init(&B.drain, 1);
     mbar_init(&B.s_free, 256), mbar_init(&B.p_ready, 256), mbar_init(&B.ds_ready, 256), mbar_init(&B.sf_init, 256);
+    mbar_init(&B.sf_ready, 256);
     mbar_init(&B.dq_free, 128);
     fence_mbar_init();
   }
@@ -674,10 +675,16 @@ __global__ void __maxnreg__(128)
         if (it + 1 < n_it && !mbar_wait(&B.q4_full, (it + 1) & 1, ctl)) break;
         if (it + 1 < n_it && it >= 1 && !mbar_wait(&B.dq_free, (it - 1) & 1, ctl)) break;
         if (!mbar_wait(&B.q_full, it & 1, ctl)) break;
+        // S(it+1) as soon as its scale factors are in place (the softmax warps
+        // write them once they have read dP(it), before computing dS(it))
+        if (it + 1 < n_it) {
+          if (!mbar_wait(&B.sf_ready, it & 1, ctl)) break;
+          tc_fence_after();
+          issue_s(it + 1);
+        }
         if (!mbar_wait(&B.ds_ready, it & 1, ctl)) break;
         const bool do_ready = it + 1 < n_it && mbar_try_wait(&B.do_full, (it + 1) & 1);
         tc_fence_after();
-        if (it + 1 < n_it) issue_s(it + 1);
         mma_dq((it & 1) * 128u);
         umma_commit(&B.dq_full);
         mma_tn(L::kDS, L::kQ, L::kColDK, it > 0);
@@ -777,6 +784,15 @@ __global__ void __maxnreg__(128)
           uint32_t v[32];
           tmem_ld32(tmem + lane_off + reg + 32 * h, v);
           if (h == 0 && it > 0) df = warp_poll(&B.ds_free, (it - 1) & 1);
+          if (h == 1 && it + 1 < n_it) {
+            // dP(it) is read: S(it+1)'s scale factors go over its last 8
+            // columns of this half, and S(it+1) may start
+            tmem_st4(tmem + lane_off + reg + L::kColSFQ, sfq);
+            tmem_st4(tmem + lane_off + reg + L::kColSFK, sfk);
+            tc_fence_before();
+            mbar_arrive(&B.sf_ready);
+            q_scales(it + 2, sfq);
+          }
 #pragma unroll
           for (int k = 0; k < 32; k += 2) {
             const float2 d = fmul2(make_float2(P[32 * h + k], P[32 * h + k + 1]),
@@ -784,12 +800,6 @@ __global__ void __maxnreg__(128)
             ds[16 * h + k / 2] = pack_bf16x2(d.x, d.y);
           }
         }
-      }
-      // dP(it) is read: S(it+1)'s scale factors go over its last 8 columns of this half
-      if (it + 1 < n_it) {
-        tmem_st4(tmem + lane_off + reg + L::kColSFQ, sfq);
-        tmem_st4(tmem + lane_off + reg + L::kColSFK, sfk);
-        q_scales(it + 2, sfq);
       }
       if (it > 0 && !warp_wait_polled(df, &B.ds_free, (it - 1) & 1, ctl)) { ok = false; break; }
       store_row64(ds_block, r, ds);
