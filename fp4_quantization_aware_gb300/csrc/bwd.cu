@@ -668,13 +668,11 @@ __global__ void __maxnreg__(128)
         ok = issue_dp_dv(0, false);
       }
       for (int it = 0; ok && it < n_it; ++it) {
-        // Inputs that are ready long before dS(it) are checked first, so that
-        // only the dS hand-off itself stands between it and the MMAs (a poll
-        // takes long while the tensor core streams shared memory). S(it+1)
-        // goes to the region dQ(it-1) used: after that is drained.
+        // Inputs of S(it+1) that are ready long before its scale factors are
+        // checked first (a poll takes long while the tensor core streams shared
+        // memory). S(it+1) goes to the region dQ(it-1) used: after that is drained.
         if (it + 1 < n_it && !mbar_wait(&B.q4_full, (it + 1) & 1, ctl)) break;
         if (it + 1 < n_it && it >= 1 && !mbar_wait(&B.dq_free, (it - 1) & 1, ctl)) break;
-        if (!mbar_wait(&B.q_full, it & 1, ctl)) break;
         // S(it+1) as soon as its scale factors are in place (the softmax warps
         // write them once they have read dP(it), before computing dS(it))
         if (it + 1 < n_it) {
@@ -682,11 +680,15 @@ __global__ void __maxnreg__(128)
           tc_fence_after();
           issue_s(it + 1);
         }
+        // the BF16 Q^ tile is needed by dK(it) only; its load follows dK(it-1)
+        const bool q_ready = mbar_try_wait(&B.q_full, it & 1);
         if (!mbar_wait(&B.ds_ready, it & 1, ctl)) break;
         const bool do_ready = it + 1 < n_it && mbar_try_wait(&B.do_full, (it + 1) & 1);
         tc_fence_after();
         mma_dq((it & 1) * 128u);
         umma_commit(&B.dq_full);
+        if (!q_ready && !mbar_wait(&B.q_full, it & 1, ctl)) break;
+        tc_fence_after();
         mma_tn(L::kDS, L::kQ, L::kColDK, it > 0);
         umma_commit(&B.q_empty);
         umma_commit(&B.ds_free);
