@@ -15,6 +15,10 @@
 // (bwd_split_plan). Both add their FP32 partial dK, dV rows into a zeroed
 // workspace slot; the one that counts second stores the BF16 sums.
 //
+// Two kernels share this structure. bwd_fp4_kernel (D = 128, described with
+// its layout below) recomputes S on the block-scaled NVFP4 MMA and gives P^
+// and dS a buffer each. bwd_kernel (D = 64) is the all-BF16 form:
+//
 // Per query tile i (all MMAs tcgen05 kind::f16, BF16 in, FP32 in TMEM):
 //   S  = Q^_i K^T        (128 columns, lane = query row)
 //   dP = dO_i V^T        (128 columns)
@@ -27,15 +31,15 @@
 // only for the softmax warps to read that step's S, and S of the next step
 // goes into the region whose dQ was drained one step earlier: the dQ drain is
 // off the critical path.
-// Warp roles (14 warps):
+// Warp roles (14 warps, both kernels):
 //   0-7  softmax: P = exp2(S*c - lse2), P^ = fake_nvfp4(P) -> smem, scale*dS -> smem
 //        (warp w reads TMEM lanes 32*(w%4).., columns [64*(w/4), +64) of a tile)
 //   8-11 dQ drain: TMEM -> FP32 swizzled smem -> TMA reduce-add into
 //        the workspace's FP32 dQ accumulator (one 32x32 box per warp and chunk)
 //   12   TMA producer (lane 0)
 //   13   MMA issuer (lane 0); the whole warp allocates and frees TMEM
-// Shared memory (D = 128): K^ 32K, V^ 32K, Q^ x2 64K, dO 32K, P^/dS 32K,
-// dQ staging 32K = 224 KiB.
+// Shared memory (D = 64): K^ 16K, V^ 16K, Q^ x2 32K, dO 16K, P^/dS 32K,
+// dQ staging 32K.
 #include "attn_common.cuh"
 #include "fp4_mma.cuh"
 
@@ -472,11 +476,15 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
 // frees one BF16 Q^ buffer (the FP4 tile feeds S, the BF16 tile only dK), so
 // P^ and dS get a 32 KiB buffer each and the softmax warps no longer wait for
 // the dK MMAs of the previous step before storing P^. MMA order per step:
-//   [dS(it) stored] S(it+1), dQ(it), dK(it), dP(it+1), [P^(it+1) stored] dV(it+1)
+//   [scale factors of S(it+1) written] S(it+1), [dS(it) stored] dQ(it), dK(it),
+//   [S(it+1) read] dP(it+1), [P^(it+1) stored] dV(it+1)
 // S(it+1) reads its scale factors from the region of dP(it): the softmax warps
-// write them there once they have read dP(it), before handing dS(it) over;
-// dQ(it), issued after S(it+1), then overwrites that region (tcgen05 MMAs of
-// one thread execute in issue order).
+// write them there once they have read dP(it), before computing dS(it), so
+// S(it+1) runs while they do; dQ(it), issued after S(it+1), then overwrites
+// that region (tcgen05 MMAs of one thread execute in issue order). Barrier
+// polls take long while the tensor core streams operands from shared memory,
+// so the waits whose phase is normally complete already (buffer releases,
+// loaded tiles) are polled early and checked late, off the hand-off path.
 // TMEM: R0 = [0,128), R1 = [128,256): S(t), dP(t), dQ(t) in R[t % 2]; the
 // scale factors of S(t) in R[(t+1) % 2] (each 64-column half h: Q scales at
 // column 56, K scales at 60, K step h); dV [256,384), dK [384,512).
