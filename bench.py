@@ -45,7 +45,7 @@ from fp4_quantization_aware_gb300 import synth  # noqa: E402
 
 PROFILE_JSON = os.path.join(ROOT, "profiles", "bwd_main_c2_counters.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "fp4_quantization_aware_gb300", "csrc", f)
-                  for f in ("bwd.cu", "attn_common.cuh", "nvfp4.cuh", "ptx.cuh")]
+                  for f in ("bwd.cu", "fp4_mma.cuh", "attn_common.cuh", "nvfp4.cuh", "ptx.cuh")]
 
 
 METRIC = "QAT attn bwd TFLOP/s on 1 GB300 (fwd in fwd_tflops); % of dense BF16 peak in roofline"
@@ -557,7 +557,7 @@ def main():
         "fwd_tflops": job_tflops(flops_f, args.steps, world, r["fwd_ms"]),
         "step_tflops": world * (flops_f + flops_b) / (r["step_ms"] * 1e-3) / 1e12,
         "bwd_ms": r["bwd_ms"] / args.steps, "fwd_ms": r["fwd_ms"] / args.steps,
-        "roofline": {"bound": "tensor", "kernel": "bwd_kernel<128> (attnqat_bwd_main)", "achieved": achieved,
+        "roofline": {"bound": "tensor", "kernel": "bwd_fp4_kernel (attnqat_bwd_main, D = 128)", "achieved": achieved,
                      "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16"],
                      "traffic": traffic, "launch_ms": main_ms,
                      "peak_note": f"{peaks['src']} dense BF16 burst (cuBLAS); sustained {peaks['bf16_sustained']}"},
