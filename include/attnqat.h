@@ -81,7 +81,9 @@ attnqat_status attnqat_check_support(const attnqat_problem* p);
  * supported). Forward: Q^, K^, V^ (BF16). Backward: Q^, K^, V^, delta (FP32,
  * B*H*Sq), an FP32 dQ accumulator (B*H*Sq*D), and FP32 partial-dK/dV slots
  * for up to 96 key tiles that the backward shares between two CTAs (the
- * preprocess step zeroes what a call uses). */
+ * preprocess step zeroes what a call uses). At D = 128 both add the NVFP4
+ * encodings of Q^ and K^ (packed E2M1 pairs and E4M3 scales, 72 bytes per
+ * row) that the S = Q^ K^T MMAs read. */
 size_t attnqat_fwd_workspace_bytes(const attnqat_problem* p);
 size_t attnqat_bwd_workspace_bytes(const attnqat_problem* p);
 
@@ -162,9 +164,9 @@ attnqat_status attnqat_fwd_r2(const attnqat_problem* p, const void* q, const voi
 attnqat_status attnqat_fwd_main_r2(const attnqat_problem* p, void* o, void* o_hp, float* lse, void* workspace,
                                    size_t workspace_bytes, void* stream);
 
-/* Backward step 1: Q^, K^, V^, delta = rowsum(O' * dO) into the workspace,
- * the FP32 dQ accumulator and the split-tile slots zeroed (one HBM-bound
- * kernel). */
+/* Backward step 1: Q^, K^, V^ (and at D = 128 their NVFP4 encodings),
+ * delta = rowsum(O' * dO) into the workspace, the FP32 dQ accumulator and the
+ * split-tile slots zeroed (one HBM-bound kernel). */
 attnqat_status attnqat_bwd_preprocess(const attnqat_problem* p, const void* dout, const void* q, const void* k,
                                       const void* v, const void* o_hp, void* workspace, size_t workspace_bytes,
                                       void* stream);
