@@ -44,9 +44,14 @@ namespace attnqat {
 namespace {
 
 constexpr int kSoftWarpsF = 16;                 // 4 per lane quarter, 32 keys of a tile each
-constexpr int kThreadsFwd = (kSoftWarpsF + 2) * 32;
-constexpr int kWarpTmaF = kSoftWarpsF;
-constexpr int kWarpMmaF = kSoftWarpsF + 1;
+constexpr int kThreadsFwd = (kSoftWarpsF + 4) * 32;
+constexpr int kWarpTmaF = kSoftWarpsF;       // SM sub-partition 0
+// The MMAs are issued from three warps on sub-partitions 1, 2 and 3: a thread
+// issuing tcgen05.mma slows the softmax warps that share its sub-partition,
+// so the issue work is spread out.
+constexpr int kWarpMmaF = kSoftWarpsF + 1;   // O' += P V^ (and TMEM allocation)
+constexpr int kWarpMmaO = kSoftWarpsF + 2;   // O += P^ V^
+constexpr int kWarpMmaS = kSoftWarpsF + 3;   // S
 
 template <int D>
 struct FwdLayout {
@@ -94,6 +99,7 @@ struct FwdBars {
   uint64_t s_full[2];
   uint64_t s_free[2];
   uint64_t p_ready[2];   // per S buffer: P and P^ of a pass-2 tile are in place
+  uint64_t pv_read[2];   // per S buffer: the O' and O MMAs of a pass-2 tile are done with it
   uint64_t o_done;       // one phase: every O' and O MMA has completed
   uint64_t ml_ready;
   uint64_t lse_ready;
@@ -142,15 +148,16 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     mbar_init(&B.q_full, 1);
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(&B.k_full[s], 1), mbar_init(&B.k_empty[s], 1);
-      mbar_init(&B.v_full[s], 1), mbar_init(&B.v_empty[s], 1);
+      mbar_init(&B.v_full[s], 1), mbar_init(&B.v_empty[s], 2);   // read by the O' and the O MMAs
     }
     for (int s = 0; s < 2; ++s) mbar_init(&B.s_full[s], 1), mbar_init(&B.s_free[s], kSoftWarpsF * 32);
     mbar_init(&B.p_ready[0], kSoftWarpsF * 32);
     mbar_init(&B.p_ready[1], kSoftWarpsF * 32);
-    mbar_init(&B.o_done, 1);
+    mbar_init(&B.pv_read[0], 2), mbar_init(&B.pv_read[1], 2);   // one commit each from the O' and O issuers
+    mbar_init(&B.o_done, 2);
     mbar_init(&B.ml_ready, 3 * 128);   // key parts 1..3
     mbar_init(&B.lse_ready, 128);      // key part 0
-    mbar_init(&B.drain, 1);
+    mbar_init(&B.drain, 3);            // one commit per MMA-issuing thread
     mbar_init(&B.sf_init, 2 * 128);    // key parts 1 and 3
     fence_mbar_init();
   }
@@ -206,8 +213,8 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         if (v_uses[s]) mbar_wait_drain(&B.v_full[s], (v_uses[s] - 1) & 1, ctl);
       }
     }
-  } else if (warp == kWarpMmaF) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == kWarpMmaF || warp == kWarpMmaO || warp == kWarpMmaS) {
+    // ------------------------------------------------------------ MMA issuers
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t kIdO = idesc_bf16(128, D, false, true);
@@ -215,74 +222,83 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       // instructions per MMA for a thread that shares its sub-partition).
       const uint64_t kmaj = sdesc_sw128(sbase, 16, 1024);
       const uint64_t mnmaj = sdesc_sw128(sbase, kBlockBytes, 1024);
-      auto issue_s = [&](int t) -> bool {
-        const int s = t & 1, ks_ = t % L::kStages;
-        // The buffer's previous tile u = t - 2 must be done with. A pass-1 S is
-        // done once the softmax warps have read it. A pass-2 buffer holds P(u),
-        // which the O' and O MMAs of tile u read; those were issued by this
-        // thread before this S MMA, and tcgen05.mma operations of one thread
-        // execute in issue order, so no wait is needed (the tensor pipe keeps
-        // running instead of draining once per tile).
-        const int u = t - 2;
-        // D = 128, pass-2 tiles from the third on: the scale factors are in the
-        // previous tile's S buffer, written there once the softmax warps have
-        // read that S (they arrive on its s_free in both passes).
-        const bool sf_in_s = L::kFp4 && t >= nk + 2;
-        const bool prev_s = u >= 0 && u < nk;   // exclusive with sf_in_s
-        uint64_t* sbar = prev_s ? &B.s_free[s] : (sf_in_s ? &B.s_free[(t - 1) & 1] : nullptr);
-        const uint32_t spar = prev_s ? ((u >> 1) & 1) : (((t - 1) >> 1) & 1);
-        if (!mbar_wait_both(&B.k_full[ks_], (t / L::kStages) & 1, sbar, spar, ctl)) return false;
-        tc_fence_after();
-        if constexpr (L::kFp4) {
-          const uint64_t d4q = sdesc_sw64(sbase + L::kQ4), d4k = sdesc_sw64(sbase + L::kK40 + ks_ * L::kFp4Tile);
-          const uint32_t sfq = sf_in_s ? L::kColS0 + ((t - 1) & 1) * 128 + L::kColSFQ2 : L::kColSFQ;
-          const uint32_t sfk = sf_in_s ? L::kColS0 + ((t - 1) & 1) * 128 + L::kColSFK2 : (s ? L::kColSFK1 : L::kColSFK0);
-          const uint32_t step = sf_in_s ? 64u : 4u;      // column distance between the K = 64 steps' factors
-#pragma unroll
-          for (int ks = 0; ks < 2; ++ks)
-            umma_nvfp4(tmem + L::kColS0 + s * 128, sdesc_advance(d4q, ks * 32), sdesc_advance(d4k, ks * 32),
-                       idesc_nvfp4(128, 128), tmem + sfq + ks * step, tmem + sfk + ks * step, ks > 0);
-        } else {
-          const uint64_t dq = sdesc_advance(kmaj, L::kQ);
-          const uint64_t db = sdesc_advance(kmaj, L::kK0 + ks_ * L::kTile);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t o = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
-            umma_bf16(tmem + L::kColS0 + s * 128, sdesc_advance(dq, o), sdesc_advance(db, o), kIdS, kk > 0);
-          }
-        }
-        umma_commit(&B.s_full[s]);
-        umma_commit(&B.k_empty[ks_]);
-        return true;
-      };
-      // O (+)= A[128 q x 128 keys] V^[128 keys x D]: A from TMEM at `a_col`
-      // (keys 32p .. 32p + 31 in columns a_col + 32p + [0,16)), V^ MN-major in
-      // shared memory.
-      auto mma_pv = [&](uint32_t a_col, uint32_t v_off, uint32_t col, bool acc) {
-        const uint64_t dv = sdesc_advance(mnmaj, v_off);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t ac = a_col + (kk >> 1) * 32 + (kk & 1) * 8;
-          umma_bf16_tmem_a(tmem + col, tmem + ac, sdesc_advance(dv, kk * 2048), kIdO, (acc || kk > 0) ? 1u : 0u);
-        }
-      };
-      bool ok = mbar_wait(&B.q_full, 0, ctl) && (!L::kFp4 || mbar_wait(&B.sf_init, 0, ctl)) && issue_s(0);
-      for (int t = 0; ok && t < nt; ++t) {
-        if (t + 1 < nt && !issue_s(t + 1)) break;
-        if (t >= nk) {
-          const int tv = t - nk, sv = tv % L::kStages;
-          // use index of this tile's S buffer among pass-2 tiles (one barrier
-          // per buffer, so the softmax warps running ahead cannot alias phases)
-          const int pr_use = (t >> 1) - ((nk + 1 - (t & 1)) >> 1);
-          if (!mbar_wait_both(&B.v_full[sv], (tv / L::kStages) & 1, &B.p_ready[t & 1], pr_use & 1, ctl)) break;
+      // use index of pass-2 tile t's S buffer among pass-2 tiles (one barrier
+      // per buffer, so the softmax warps running ahead cannot alias phases)
+      auto pr_use = [&](int t) { return (t >> 1) - ((nk + 1 - (t & 1)) >> 1); };
+      bool ok = true;
+      if (warp == kWarpMmaS) {
+        auto issue_s = [&](int t) -> bool {
+          const int s = t & 1, ks_ = t % L::kStages;
+          // The buffer's previous tile u = t - 2 must be done with: a pass-1 S
+          // once the softmax warps have read it, a pass-2 buffer (P(u), P^(u))
+          // once the O' and O MMAs of tile u have completed.
+          const int u = t - 2;
+          // D = 128, pass-2 tiles from the third on: the scale factors are in the
+          // previous tile's S buffer, written there once the softmax warps have
+          // read that S (they arrive on its s_free in both passes).
+          const bool sf_in_s = L::kFp4 && t >= nk + 2;
+          const bool prev_s = u >= 0 && u < nk;   // exclusive with sf_in_s
+          uint64_t* sbar = prev_s ? &B.s_free[s] : (sf_in_s ? &B.s_free[(t - 1) & 1] : nullptr);
+          const uint32_t spar = prev_s ? ((u >> 1) & 1) : (((t - 1) >> 1) & 1);
+          const bool pv_wait = u >= nk;
+          const bool kf = mbar_try_wait(&B.k_full[ks_], (t / L::kStages) & 1);
+          if (!mbar_wait_both(sbar, spar, pv_wait ? &B.pv_read[s] : nullptr, pv_wait ? (pr_use(u) & 1) : 0u, ctl))
+            return false;
+          if (!kf && !mbar_wait(&B.k_full[ks_], (t / L::kStages) & 1, ctl)) return false;
           tc_fence_after();
-          const uint32_t vb = L::kV0 + sv * L::kTile;
+          if constexpr (L::kFp4) {
+            const uint64_t d4q = sdesc_sw64(sbase + L::kQ4), d4k = sdesc_sw64(sbase + L::kK40 + ks_ * L::kFp4Tile);
+            const uint32_t sfq = sf_in_s ? L::kColS0 + ((t - 1) & 1) * 128 + L::kColSFQ2 : L::kColSFQ;
+            const uint32_t sfk = sf_in_s ? L::kColS0 + ((t - 1) & 1) * 128 + L::kColSFK2 : (s ? L::kColSFK1 : L::kColSFK0);
+            const uint32_t step = sf_in_s ? 64u : 4u;      // column distance between the K = 64 steps' factors
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks)
+              umma_nvfp4(tmem + L::kColS0 + s * 128, sdesc_advance(d4q, ks * 32), sdesc_advance(d4k, ks * 32),
+                         idesc_nvfp4(128, 128), tmem + sfq + ks * step, tmem + sfk + ks * step, ks > 0);
+          } else {
+            const uint64_t dq = sdesc_advance(kmaj, L::kQ);
+            const uint64_t db = sdesc_advance(kmaj, L::kK0 + ks_ * L::kTile);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t o = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
+              umma_bf16(tmem + L::kColS0 + s * 128, sdesc_advance(dq, o), sdesc_advance(db, o), kIdS, kk > 0);
+            }
+          }
+          umma_commit(&B.s_full[s]);
+          umma_commit(&B.k_empty[ks_]);
+          return true;
+        };
+        ok = mbar_wait(&B.q_full, 0, ctl) && (!L::kFp4 || mbar_wait(&B.sf_init, 0, ctl));
+        for (int t = 0; ok && t < nt; ++t) ok = issue_s(t);
+      } else {
+        // O' += P V^ (warp kWarpMmaF) or O += P^ V^ (warp kWarpMmaO) for every
+        // pass-2 tile, A from TMEM at the tile's S buffer (keys 32p .. 32p + 31
+        // in columns 32p + [0,16) for P and 32p + [16,32) for P^), V^ MN-major
+        // in shared memory. D = 128: the P^ of each key half's last 16 keys
+        // comes from shared memory (its TMEM columns hold the next S's scale
+        // factors).
+        const bool is_op = warp == kWarpMmaF;
+        // The scale factors of pass 1 and of pass-2 tiles 0, 1 sit in the O'
+        // columns: the first O' MMA waits until S of those tiles has completed.
+        if (is_op && L::kFp4 && nk < nt) {
+          const int t0 = nk, t1 = nk + 1;
+          ok = mbar_wait_both(&B.s_full[t0 & 1], (t0 >> 1) & 1, t1 < nt ? &B.s_full[t1 & 1] : nullptr,
+                              (t1 >> 1) & 1, ctl);
+        }
+        for (int t = nk; ok && t < nt; ++t) {
+          const int tv = t - nk, sv = tv % L::kStages;
+          if (!mbar_wait_both(&B.v_full[sv], (tv / L::kStages) & 1, &B.p_ready[t & 1], pr_use(t) & 1, ctl)) break;
+          tc_fence_after();
+          const uint64_t dv = sdesc_advance(mnmaj, L::kV0 + sv * L::kTile);
           const uint32_t sc = L::kColS0 + (t & 1) * 128;
-          mma_pv(sc, vb, L::kColOP, tv > 0);        // O' += P V^
-          // O += P^ V^. D = 128: the P^ of each key half's last 16 keys comes
-          // from shared memory (its TMEM columns hold the next S's scale factors)
-          {
-            const uint64_t dv = sdesc_advance(mnmaj, vb);
+          if (is_op) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t ac = sc + (kk >> 1) * 32 + (kk & 1) * 8;
+              umma_bf16_tmem_a(tmem + L::kColOP, tmem + ac, sdesc_advance(dv, kk * 2048), kIdO,
+                               (tv > 0 || kk > 0) ? 1u : 0u);
+            }
+          } else {
             const uint64_t dl = sdesc_advance(kmaj, L::kPL0 + (tv & 1) * 2 * kBlockBytes);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
@@ -297,6 +313,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             }
           }
           umma_commit(&B.v_empty[sv]);
+          umma_commit(&B.pv_read[t & 1]);
           if (tv == nk - 1) umma_commit(&B.o_done);
         }
       }
