@@ -37,9 +37,12 @@
 namespace attnqat {
 namespace {
 
-constexpr int kWarpTmaI = 8;
-constexpr int kWarpMmaI = 9;
-constexpr int kThreadsInf = 10 * 32;
+constexpr int kWarpTmaI = 8;    // SM sub-partition 0
+// A thread issuing tcgen05.mma slows the softmax warps of its sub-partition:
+// PV and S come from warps on two different ones.
+constexpr int kWarpMmaI = 9;    // PV (and TMEM allocation), sub-partition 1
+constexpr int kWarpMmaS = 10;   // S, sub-partition 2
+constexpr int kThreadsInf = 11 * 32;
 constexpr int kD = 128;
 constexpr int kStagesK = 3;
 constexpr int kStagesV = 3;
@@ -74,6 +77,7 @@ struct InfBars {
   uint64_t s_full[2];
   uint64_t p_ready[2];    // P(j) is in TMEM over S(j), and the K scales of tile j + 2
   uint64_t pv_done;       // one phase per PV(j) (waited only before rescaling O)
+  uint64_t pv_read[2];    // per S buffer: PV(j) is done with P(j)
   uint64_t o_done;
   uint64_t drain;
   uint32_t tmem_base;
@@ -94,7 +98,8 @@ struct InfArgs {
   uint64_t timeout_ns;
 };
 
-__global__ void __launch_bounds__(kThreadsInf, 1)
+// Three warps share SM sub-partitions 0-2: at most 168 registers a thread.
+__global__ void __maxnreg__(168)
     infer_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const InfArgs a) {
   using L = InfLayout;
@@ -120,8 +125,9 @@ __global__ void __launch_bounds__(kThreadsInf, 1)
     for (int s = 0; s < kStagesV; ++s) mbar_init(&B.v_full[s], 1), mbar_init(&B.v_empty[s], 1);
     for (int s = 0; s < 2; ++s) mbar_init(&B.s_full[s], 1), mbar_init(&B.p_ready[s], 256);
     mbar_init(&B.pv_done, 1);
+    mbar_init(&B.pv_read[0], 1), mbar_init(&B.pv_read[1], 1);
     mbar_init(&B.o_done, 1);
-    mbar_init(&B.drain, 1);
+    mbar_init(&B.drain, 2);   // one commit per MMA-issuing thread
     fence_mbar_init();
   }
   if (warp == kWarpMmaI) {
@@ -169,17 +175,19 @@ __global__ void __launch_bounds__(kThreadsInf, 1)
       for (int s = 0; s < kStagesV; ++s)
         if (v_uses[s]) mbar_wait_drain(&B.v_full[s], (v_uses[s] - 1) & 1, ctl);
     }
-  } else if (warp == kWarpMmaI) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == kWarpMmaS) {
+    // ------------------------------------------------------------ S issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_nvfp4(128, 128);
-      constexpr uint32_t kIdO = idesc_bf16(128, kD, false, true);
       const uint64_t dq = sdesc_sw64(sbase + L::kQ);
-      const uint64_t mnmaj = sdesc_sw128(sbase, kBlockBytes, 1024);
-      // S(j); `ready`: an earlier poll already saw K(j) loaded
-      auto issue_s = [&](int j, bool ready) -> bool {
+      bool ok = mbar_wait(&B.q_full, 0, ctl) && mbar_wait(&B.sf_init, 0, ctl);
+      for (int j = 0; ok && j < nk; ++j) {
         const int s = j % kStagesK, b = j & 1;
-        if (!ready && !mbar_wait(&B.k_full[s], (j / kStagesK) & 1, ctl)) return false;
+        // S(j) goes over P(j-2): once PV(j-2) is done with it. The K scales of
+        // tile j were written with P(j-2) (p_ready). The polls overlap.
+        const bool kf = mbar_try_wait(&B.k_full[s], (j / kStagesK) & 1);
+        if (j >= 2 && !mbar_wait_both(&B.pv_read[b], ((j - 2) >> 1) & 1, &B.p_ready[b], ((j - 2) >> 1) & 1, ctl)) break;
+        if (!kf && !mbar_wait(&B.k_full[s], (j / kStagesK) & 1, ctl)) break;
         tc_fence_after();
         const uint64_t dk = sdesc_sw64(sbase + L::kK + s * L::kFp4Tile);
         const uint32_t sfk = b ? L::kColSFK1 : L::kColSFK0;
@@ -189,14 +197,18 @@ __global__ void __launch_bounds__(kThreadsInf, 1)
                      tmem + L::kColSFQ + ks * 4, tmem + sfk + ks * 4, ks > 0);
         umma_commit(&B.s_full[b]);
         umma_commit(&B.k_empty[s]);
-        return true;
-      };
-      bool ok = mbar_wait(&B.q_full, 0, ctl) && mbar_wait(&B.sf_init, 0, ctl) && issue_s(0, false) &&
-                (nk < 2 || issue_s(1, false));
+      }
+      umma_commit(&B.drain);
+      mbar_wait_drain(&B.drain, 0, ctl);
+    }
+  } else if (warp == kWarpMmaI) {
+    // ------------------------------------------------------------ PV issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdO = idesc_bf16(128, kD, false, true);
+      const uint64_t mnmaj = sdesc_sw128(sbase, kBlockBytes, 1024);
+      bool ok = true;
       for (int j = 0; ok && j < nk; ++j) {
         const int sv = j % kStagesV, b = j & 1;
-        // K(j+2) is polled together with V(j) and P(j) (overlapping polls)
-        const bool k_ready = j + 2 < nk && mbar_try_wait(&B.k_full[(j + 2) % kStagesK], ((j + 2) / kStagesK) & 1);
         if (!mbar_wait_both(&B.v_full[sv], (j / kStagesV) & 1, &B.p_ready[b], (j >> 1) & 1, ctl)) break;
         tc_fence_after();
         const uint64_t dv = sdesc_advance(mnmaj, L::kV + sv * L::kVTile);
@@ -207,8 +219,8 @@ __global__ void __launch_bounds__(kThreadsInf, 1)
                            kIdO, (j > 0 || kk > 0) ? 1u : 0u);
         umma_commit(&B.v_empty[sv]);
         umma_commit(&B.pv_done);
+        umma_commit(&B.pv_read[b]);
         if (j == nk - 1) umma_commit(&B.o_done);
-        if (j + 2 < nk && !issue_s(j + 2, k_ready)) break;
       }
       umma_commit(&B.drain);
       mbar_wait_drain(&B.drain, 0, ctl);
