@@ -19,9 +19,11 @@
 // back over the S tile they read: the warps of key part p (keys 32p..32p+31)
 // put P in columns 32p + [0,16) and P^ in 32p + [16,32) of that S buffer,
 // columns only they read, and the O' and O MMAs take their A operand from
-// TMEM there. The next S goes into a buffer once the MMAs reading its P are
-// done (issue order). Warp roles (18 warps): 0-15 softmax (warp w: lanes
-// 32*(w%4).., key columns [32*(w/4), +32)); 16 TMA producer; 17 MMA issuer.
+// TMEM there. The next S goes into a buffer once the O' and O MMAs reading
+// its P and P^ have completed (their commits). Warp roles (20 warps): 0-15
+// softmax (warp w: lanes 32*(w%4).., key columns [32*(w/4), +32)); 16 TMA
+// producer; 17, 18, 19 MMA issuers of O', O and S, one per SM sub-partition
+// 1-3 (an issuing thread slows the softmax warps of its own sub-partition).
 // K^ and V^ tiles are triple-buffered in shared memory.
 //
 // D = 128: both passes compute S on the block-scaled NVFP4 tensor-core MMA
@@ -370,7 +372,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       uint32_t v[32];
       tmem_ld32(tmem + lane_off + L::kColS0 + s * 128 + part * 32, v);
       // tile t + 2's K scales into the slot S(t) used (S(t) is complete);
-      // releasing S(t) below also certifies them to the MMA issuer
+      // releasing S(t) below also certifies them to the S issuer
       if (more) tmem_st4(tmem + lane_off + (s ? L::kColSFK1 : L::kColSFK0) + 4 * ks, sfw);
       tc_fence_before();
       mbar_arrive(&B.s_free[s]);
@@ -435,7 +437,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       }
     }
 
-    // pass 2: P = exp2(S * c2 - lse2), P^ = fake_nvfp4(P); hand both to the MMA warp
+    // pass 2: P = exp2(S * c2 - lse2), P^ = fake_nvfp4(P); hand both to the MMA warps
     uint32_t sfq[4] = {0u, 0u, 0u, 0u};   // D = 128: K step ks of the Q scale factors (parts 1, 3)
     if (L::kFp4 && sf_writer)
       load_scales(a.q_sf, static_cast<int64_t>(bh) * a.Sq + i * 128, min(128, a.Sq - i * 128), ks, sfq);

@@ -22,15 +22,15 @@
 // query rows) and key half w / 4 (64 of the tile's 128 keys). The two warps of
 // a quarter exchange their half-row maxima through shared memory once per
 // tile (a 64-thread named barrier), so both take the same rescaling decision.
-// Tensor-pipe order: S(0) S(1) PV(0) S(2) PV(1) S(3) ...; tcgen05 MMAs from one
-// thread execute in issue order, so S(j+2) overwrites buffer j % 2 only after
-// PV(j) has read P(j) from it.
+// S and PV are issued by two threads (on different SM sub-partitions, as an
+// issuing thread slows the softmax warps of its own): S(j+2) overwrites buffer
+// j % 2 once PV(j), which read P(j) from it, has completed (its commit).
 //
 // The block-scaled MMA's operand and scale-factor layouts are in fp4_mma.cuh.
 //
 // TMEM columns: S0 [0,128), S1 [128,256), O [256,384), Q scales [384,392),
 // K scales x2 [400,408) and [416,424). Warps: 0-7 softmax, 8 TMA producer,
-// 9 MMA issuer.
+// 9 PV issuer, 10 S issuer.
 #include "attn_common.cuh"
 #include "fp4_mma.cuh"
 
