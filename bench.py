@@ -93,8 +93,8 @@ def measured_peaks() -> dict:
     if os.path.exists(p):
         d = json.load(open(p))
         return {"bf16": d["bf16_tflops"], "bf16_sustained": d.get("bf16_tflops_sustained"), "hbm": d["hbm_gbs"],
-                "src": "measured"}
-    return {"bf16": 1900.0, "bf16_sustained": 1700.0, "hbm": 6800.0, "src": "fallback"}
+                "sm_max_mhz": d.get("sm_max_mhz", 2070.0), "src": "measured"}
+    return {"bf16": 1900.0, "bf16_sustained": 1700.0, "hbm": 6800.0, "sm_max_mhz": 2070.0, "src": "fallback"}
 
 
 class ClockSampler:
@@ -336,7 +336,8 @@ def run_infer(args, w, rank, world, local_rank):
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = sum(v.numel() * v.element_size() for v in host_out)
     res = {"step_ms": step_ms, "kern_ms": kern_ms, "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h,
-           "launches": 3 * args.steps, "clocks": clk.summary()}
+           "launches": 3 * args.steps, "clocks": clk.summary(),
+           "n_sm": torch.cuda.get_device_properties(dev).multi_processor_count}
     res["step_ms"], res["e2e_ms"] = max_over_ranks([step_ms, e2e_ms], dev)
     return res
 
@@ -345,8 +346,9 @@ def infer_line(args, w, world, r, peaks, l2) -> dict:
     flops = w.fwd_flops()
     kern_ms = statistics.mean(r["kern_ms"])
     exps = w.B * w.H * w.Sq * w.Sk / (2 if w.causal else 1)
-    sm_mhz = 2070.0
-    mufu_peak = MUFU_EX2_PER_CLK_SM * 152 * sm_mhz * 1e6 / 1e9            # G exp2/s at the maximum SM clock
+    sm_mhz = peaks["sm_max_mhz"]
+    n_sm = r["n_sm"]
+    mufu_peak = MUFU_EX2_PER_CLK_SM * n_sm * sm_mhz * 1e6 / 1e9           # G exp2/s at the maximum SM clock
     achieved = exps / (kern_ms * 1e-3) / 1e9
     # tensor-pipe bound: half the FLOPs (QK) at the FP4 rate, half (PV) at the BF16 rate
     tensor_peak = 2.0 / (1.0 / peaks["bf16"] + 1.0 / (FP4_OVER_BF16 * peaks["bf16"]))
@@ -367,7 +369,8 @@ def infer_line(args, w, world, r, peaks, l2) -> dict:
         "roofline": {"bound": "alu", "kernel": "infer_kernel (attnqat_infer_fwd_packed)", "achieved": achieved,
                      "peak": mufu_peak, "unit": "Gexp2/s", "frac": achieved / mufu_peak, "traffic": traffic,
                      "launch_ms": kern_ms,
-                     "peak_note": f"MUFU ex2: {MUFU_EX2_PER_CLK_SM}/clk/SM x 152 SMs x {sm_mhz:.0f} MHz (derived)",
+                     "peak_note": f"MUFU ex2: {MUFU_EX2_PER_CLK_SM}/clk/SM x {n_sm} SMs (device) x {sm_mhz:.0f} MHz "
+                                  f"(sm_max_mhz, {peaks['src']}): derived",
                      "tensor": {"achieved": tensor_achieved, "peak": tensor_peak, "unit": "TFLOP/s",
                                 "frac": tensor_achieved / tensor_peak,
                                 "note": f"QK at {FP4_OVER_BF16:g}x and PV at 1x the {peaks['src']} BF16 peak "

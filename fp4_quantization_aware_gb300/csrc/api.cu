@@ -6,6 +6,8 @@
 #include <cstring>
 #include <initializer_list>
 
+#include <mutex>
+
 #include "../../include/attnqat.h"
 #include "attn_common.cuh"
 
@@ -101,7 +103,11 @@ attnqat_status check_ws(const void* ws, size_t bytes, size_t need) {
   return ATTNQAT_OK;
 }
 
+// The device address of g_device_error, looked up once per device (under a
+// lock: calls may come from several host threads) and cached for the life of
+// the CUDA context.
 uint32_t* device_error_word(attnqat_status* st) {
+  static std::mutex lock;
   static uint32_t* cache[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -109,6 +115,7 @@ uint32_t* device_error_word(attnqat_status* st) {
     *st = cuda_fail(e, "cudaGetDevice");
     return nullptr;
   }
+  std::lock_guard<std::mutex> guard(lock);
   if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
   void* p = nullptr;
   e = cudaGetSymbolAddress(&p, g_device_error);

@@ -5,23 +5,30 @@
 // device allocation is not allowed or not possible (a host callback, a runtime
 // that forbids cudaMalloc after start-up, an embedding with its own fixed
 // memory budget and no allocator hook). This entry point gives them the
-// backward with its scratch space (Q^, K^, V^, delta and the FP32 dQ
-// accumulator) in a statically sized device array that the library declares
-// itself, so the call allocates nothing.
+// backward with its scratch space (Q^, K^, V^ and their NVFP4 encodings,
+// delta, the FP32 dQ accumulator, the split-tile counters and dK/dV slots) in
+// a statically sized device array that the library declares itself, so the
+// call allocates nothing.
 //
 // Limits and sharing:
 //  - The array holds kNoAllocScratchBytes (32 MiB). A problem whose
 //    attnqat_bwd_workspace_bytes() exceeds it is rejected with
 //    ATTNQAT_ERR_WORKSPACE before anything is enqueued.
-//  - Every GPU that loads the library holds the array until the process exits.
+//  - Every GPU that loads this module holds the array until the process exits.
 //  - All calls on a device share the one array and it keeps the last call's
-//    contents. The dQ accumulator, the only part that must start at zero, is
+//    contents. The parts that must start at zero (the FP32 dQ accumulator, the
+//    split-tile counters and the FP32 dK/dV slots of split tiles) are all
 //    cleared by the preprocess step of every call. Calls whose executions
 //    overlap on the GPU (different streams, or different host threads without
 //    ordering between them) race on the array and give wrong results.
 //  - The first call on each device looks up the array's device address with
-//    cudaGetSymbolAddress (with that device current); make that first call
-//    before any stream capture.
+//    cudaGetSymbolAddress (with that device current). Under CUDA's lazy module
+//    loading (the default since CUDA 12.2) this lookup is what loads the
+//    module and reserves the 32 MiB, so the first call can fail with
+//    ATTNQAT_ERR_CUDA on a full device: make it at start-up, before any stream
+//    capture and before a memory budget applies.
+//  - The address is cached per device index for the life of the CUDA context;
+//    a device reset (cudaDeviceReset) between calls would leave it stale.
 #include <mutex>
 
 #include "../../include/attnqat.h"

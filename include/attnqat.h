@@ -188,11 +188,17 @@ attnqat_status attnqat_bwd_dq_convert(const attnqat_problem* p, void* dq, void* 
  * that such callers need no workspace. It computes exactly what attnqat_bwd
  * computes, with the scratch space in a 32 MiB static device array that the
  * library declares; problems whose attnqat_bwd_workspace_bytes() exceed
- * 32 MiB return ATTNQAT_ERR_WORKSPACE. It allocates nothing. Every GPU that
- * loads the library holds the array until exit; all calls share it and it
- * keeps the last call's contents, so calls that overlap on the GPU race.
- * The first call on a device looks up the array's address (make it before any
- * stream capture). */
+ * 32 MiB return ATTNQAT_ERR_WORKSPACE. It calls no allocator. Every GPU that
+ * loads the library's module holds the array until exit; all calls share it
+ * and it keeps the last call's contents (each call's preprocess clears the
+ * parts that must start at zero), so calls that overlap on the GPU race.
+ * The first call on a device looks up the array's address. Under CUDA's lazy
+ * module loading (the default) that lookup is also what loads the module and
+ * reserves the 32 MiB on that device, so the first call can fail with
+ * ATTNQAT_ERR_CUDA when the device is full: make it at start-up, before any
+ * stream capture and before a memory budget applies. The address is cached
+ * per device for the life of the CUDA context: do not reset the device
+ * (cudaDeviceReset) between calls. */
 attnqat_status attnqat_bwd_noalloc(const attnqat_problem* p, const void* dout, const void* q, const void* k,
                                    const void* v, const void* o_hp, const float* lse, void* dq, void* dk, void* dv,
                                    void* stream);

@@ -309,7 +309,3 @@ def nvfp4_codes(x, axis=-1):
                   np.rint(s / 2.0 ** -9).astype(np.int64))
     return np.moveaxis(codes, -1, axis), np.moveaxis(sc.astype(np.uint8), -1, axis)
 
-
-def delta(o_hp, do):
-    """The backward's preprocessing statistic rowsum(O' * dO), float64."""
-    return np.sum(np.asarray(o_hp, np.float64) * np.asarray(do, np.float64), axis=-1)

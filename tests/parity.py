@@ -4,6 +4,7 @@ import numpy as np
 REL_TOL = 1e-2          # relative Frobenius error bound on O, O', dQ, dK, dV
 COS_TOL = 0.999         # cosine similarity bound
 LSE_TOL = 1e-3          # max abs error of the natural-log LSE
+TILE_ROWS = 128         # rows per block of the per-tile checks (the kernels' tile)
 
 
 def rel_cos(got, ref):
@@ -17,10 +18,31 @@ def rel_cos(got, ref):
     return rel, cos
 
 
-def assert_close(name, got, ref, rel_tol=REL_TOL, cos_tol=COS_TOL):
+def assert_close(name, got, ref, rel_tol=REL_TOL, cos_tol=COS_TOL, tile=TILE_ROWS):
+    """The bounds over the whole tensor, then over every `tile`-row block of
+    each head (axis -2 holds the rows), the granularity at which the kernels
+    own their outputs: one wrong row or tile cannot hide under the norm of
+    the rest. A block whose reference is exactly zero must be exactly zero."""
     rel, cos = rel_cos(got, ref)
     assert rel <= rel_tol and cos >= cos_tol, f"{name}: rel={rel:.3e} cos={cos:.6f}"
+    assert_tiles(name, got, ref, rel_tol, cos_tol, tile)
     return rel, cos
+
+
+def assert_tiles(name, got, ref, rel_tol=REL_TOL, cos_tol=COS_TOL, tile=TILE_ROWS):
+    g = np.asarray(got, np.float64)
+    r = np.asarray(ref, np.float64)
+    assert g.shape == r.shape, f"{name}: shape {g.shape} != {r.shape}"
+    if g.ndim < 2:
+        return
+    n = g.shape[-2]
+    g = g.reshape(-1, n, g.shape[-1])
+    r = r.reshape(-1, n, r.shape[-1])
+    for h in range(g.shape[0]):
+        for t0 in range(0, n, tile):
+            rel, cos = rel_cos(g[h, t0:t0 + tile], r[h, t0:t0 + tile])
+            assert rel <= rel_tol and cos >= cos_tol, \
+                f"{name}: head {h} rows [{t0}, {min(n, t0 + tile)}): rel={rel:.3e} cos={cos:.6f}"
 
 
 def to_dev(a, dtype=None):

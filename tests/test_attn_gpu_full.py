@@ -1,6 +1,7 @@
 """CUDA Attn-QAT at the full workload sizes against the float64 oracle.
 
-c2 (B=1 H=16 S=4096 D=128) is compared in full on every head. c3, c4 and c5
+c2 (B=1 H=16 S=4096 D=128) is compared in full on every head, over each
+whole head and over each 128-row tile of it. c3, c4 and c5
 are too large for a whole-tensor float64 oracle, so the first and the last
 (b, h) head are checked on sampled outputs the oracle computes one block at
 a time: three 64-row query blocks (start, middle, the ragged end) for O, O',
@@ -15,7 +16,7 @@ import pytest
 
 import oracle
 from fp4_quantization_aware_gb300 import attnqat, synth
-from parity import LSE_TOL, REL_TOL, COS_TOL, bf16_dev, rel_cos, round_bf16, to_dev
+from parity import LSE_TOL, REL_TOL, COS_TOL, assert_tiles, bf16_dev, rel_cos, round_bf16, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -24,6 +25,7 @@ def _check(name, got, ref, report):
     rel, cos = rel_cos(got, ref)
     report.append(f"{name}: rel={rel:.2e} cos={cos:.6f} |ref|={np.linalg.norm(ref):.3e}")
     assert rel <= REL_TOL and cos >= COS_TOL, "\n".join(report)
+    assert_tiles(name, got, ref)   # every 128-row tile of a whole head (the sampled blocks are 64 rows)
 
 
 def _blocks(n, size=64, align=16):

@@ -27,14 +27,26 @@ def test_bwd_noalloc_matches_workspace_backward(lib):
     torch.cuda.synchronize()
     ref = [host(t) for t in ref]
     stream = torch.cuda.current_stream().cuda_stream
+    outs = [[torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)] for _ in range(2)]
+    torch.cuda.synchronize()
+    mem0 = torch.cuda.memory_allocated()
     for call in range(2):
-        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        dq, dk, dv = outs[call]
         st = lib.attnqat_bwd_noalloc(ctypes.byref(p), do.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(),
                                      o_hp.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
                                      stream)
         attnqat.check(st, "attnqat_bwd_noalloc")
         torch.cuda.synchronize()
-        for name, got, want in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+        # the call allocates nothing: torch's allocator and the device's free
+        # memory stay where the first call (which may load the array's module)
+        # left them
+        if call == 0:
+            free0 = torch.cuda.mem_get_info()[0]
+        else:
+            assert torch.cuda.mem_get_info()[0] == free0
+        assert torch.cuda.memory_allocated() == mem0
+    for call in range(2):
+        for name, got, want in zip(("dQ", "dK", "dV"), outs[call], ref):
             assert_close(f"call {call} {name}", host(got), want)
     assert attnqat.device_status() == 0
 
