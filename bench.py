@@ -16,7 +16,14 @@ the float64 CPU oracle on whole heads of the same workload (about 10 s).
 
 With --gpus N (launched by torchrun) every rank runs the full workload on its
 own GPU (independent problems, no collective on the data path) and `value` is
-the sum over ranks divided by the slowest rank's time (weak scaling).
+the sum over ranks divided by the slowest rank's time (weak scaling). With
+--shard heads the ranks instead split one workload's B*H heads into
+contiguous, balanced slices (every (b, h) head is independent in both
+directions, and a slice of the flattened heads is contiguous in BHSD), each
+rank generating and running only its own slice; `value` is the whole
+workload's FLOPs over the slowest rank's time (strong scaling). Neither mode
+has a collective on the data path: only the timing barrier and the max over
+ranks use the process group.
 
 --workload ctx32k (or --path infer) measures the NVFP4 inference forward
 instead: a step is NVFP4 packing of Q and K plus the block-scaled FP4 QK /
@@ -76,9 +83,46 @@ def max_over_ranks(values, device=None):
 
 
 def job_tflops(flops_per_rank_step: float, steps: int, world: int, max_ms: float) -> float:
-    """Whole-job throughput: every rank does the same work (weak scaling), the
-    job takes as long as its slowest rank."""
+    """Whole-job throughput: `world` ranks each doing `flops_per_rank_step`
+    (pass world = 1 with the whole job's FLOPs when the ranks split one
+    workload); the job takes as long as its slowest rank."""
     return world * flops_per_rank_step * steps / (max_ms * 1e-3) / 1e12
+
+
+def head_slice(n_heads: int, world: int, rank: int) -> tuple[int, int]:
+    """The heads [h0, h1) of the flattened (b, h) order that rank `rank` of
+    `world` takes in the data-parallel mode: contiguous, sizes differing by at
+    most one, every head in exactly one rank's slice."""
+    if world < 1 or not 0 <= rank < world:
+        raise ValueError(f"rank {rank} of {world}")
+    return rank * n_heads // world, (rank + 1) * n_heads // world
+
+
+def shard_heads(w, world: int, rank: int) -> list:
+    """The (b, h) pairs of this rank's slice, in BHSD memory order."""
+    n = w.B * w.H
+    if world > n:
+        raise ValueError(f"--shard heads needs at most B*H = {n} ranks, got {world}")
+    h0, h1 = head_slice(n, world, rank)
+    return [divmod(i, w.H) for i in range(h0, h1)]
+
+
+def shard_byte_offsets(w, rank_heads: list) -> dict:
+    """Byte offset of a slice's first head in each full BHSD tensor (and in
+    the (B, H, Sq) LSE), for a caller that keeps the whole tensors and hands
+    each rank a view: the slice is contiguous there."""
+    b, h = rank_heads[0]
+    i = b * w.H + h
+    return {"q": i * w.Sq * w.D * 2, "do": i * w.Sq * w.D * 2, "o": i * w.Sq * w.D * 2,
+            "k": i * w.Sk * w.D * 2, "v": i * w.Sk * w.D * 2, "lse": i * w.Sq * 4}
+
+
+def rank_workload(w, heads):
+    """The workload one rank runs: the whole one, or its slice of heads as a
+    (len(heads), 1) batch (each head is an independent problem)."""
+    if heads is None:
+        return w
+    return synth.workload(w.name, B=len(heads), H=1, Sq=w.Sq, Sk=w.Sk)
 
 
 def kernel_hash(sources=None) -> str:
@@ -154,7 +198,9 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------- ours
-def run_ours(args, w, rank, world, local_rank):
+def run_ours(args, w, rank, world, local_rank, heads=None):
+    """Time the QAT step on the whole workload, or on `heads` (this rank's
+    slice, generated head by head exactly as in the whole workload)."""
     import torch
     from fp4_quantization_aware_gb300 import attnqat
     import ctypes
@@ -162,7 +208,8 @@ def run_ours(args, w, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     lib = attnqat.load()
-    x = synth.inputs(w)
+    x = synth.inputs(w, heads=heads)
+    w = rank_workload(w, heads)
     t = {n: torch.from_numpy(a).to(torch.bfloat16).to(dev) for n, a in x.items()}
     p = attnqat.problem(w.B, w.H, w.Sq, w.Sk, w.D, w.causal, w.scale)
     pp = ctypes.byref(p)
@@ -458,6 +505,9 @@ def main():
                     help="qat: the QAT forward+backward step; infer: the NVFP4 inference forward "
                          "(default: infer for ctx32k, qat otherwise)")
     ap.add_argument("--seq", type=int, default=None, help="override Sq = Sk of the workload (smaller captures)")
+    ap.add_argument("--shard", default="none", choices=["none", "heads"],
+                    help="with --gpus N: none = every rank runs the whole workload (weak scaling); heads = the "
+                         "ranks split its B*H heads into contiguous slices (strong scaling)")
     ap.add_argument("--recipe", default="standard", choices=["standard", "r2"],
                     help="forward recipe of the QAT step: standard (two passes, P^ of the normalised P) or r2 "
                          "(one pass, P^ of each key tile's unnormalised P)")
@@ -539,32 +589,43 @@ def main():
         if world > 1:
             torch.distributed.destroy_process_group()
         return
-    r = run_ours(args, w, rank, world, local_rank)
+    heads = shard_heads(w, world, rank) if args.shard == "heads" else None
+    r = run_ours(args, w, rank, world, local_rank, heads)
     if rank != 0:
         torch.distributed.destroy_process_group()
         return
-    flops_b, flops_f = w.bwd_flops(), w.fwd_flops()
-    value = job_tflops(flops_b, args.steps, world, r["bwd_ms"])
+    wr = rank_workload(w, heads)               # what rank 0 ran
+    # whole-job FLOPs per step: the one workload split over the ranks, or one
+    # copy of it per rank
+    job = 1 if heads is not None else world
+    flops_b, flops_f = job * w.bwd_flops(), job * w.fwd_flops()
+    value = job_tflops(flops_b, args.steps, 1, r["bwd_ms"])
     main_ms = statistics.mean(r["main_ms"])
-    achieved = flops_b / (main_ms * 1e-3) / 1e12
+    achieved = wr.bwd_flops() / (main_ms * 1e-3) / 1e12
     traffic = None
     if os.path.exists(PROFILE_JSON):
         prof = json.load(open(PROFILE_JSON))
-        if prof.get("kernel_hash") == kernel_hash() and prof.get("workload") == w.name:
+        if prof.get("kernel_hash") == kernel_hash() and prof.get("workload") == w.name and heads is None:
             traffic = prof.get("dram_bytes_per_launch")
+    cfg = workload_config(w, l2, args.recipe)
+    if world > 1:
+        cfg["parallelism"] = (f"data parallel over B*H heads: {world} contiguous slices, rank 0 "
+                              f"heads {heads[0]}..{heads[-1]}" if heads is not None
+                              else f"{world} replicas of the whole workload")
     line = {
         "metric": METRIC,
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": r["step_ms"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic", "config": workload_config(w, l2, args.recipe),
-        "fwd_tflops": job_tflops(flops_f, args.steps, world, r["fwd_ms"]),
-        "step_tflops": world * (flops_f + flops_b) / (r["step_ms"] * 1e-3) / 1e12,
+        "ms_per_step": r["step_ms"], "higher_is_better": True,
+        "scaling": "strong" if heads is not None else "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic", "config": cfg,
+        "fwd_tflops": job_tflops(flops_f, args.steps, 1, r["fwd_ms"]),
+        "step_tflops": (flops_f + flops_b) / (r["step_ms"] * 1e-3) / 1e12,
         "bwd_ms": r["bwd_ms"] / args.steps, "fwd_ms": r["fwd_ms"] / args.steps,
         "roofline": {"bound": "tensor", "kernel": "bwd_fp4_kernel (attnqat_bwd_main, D = 128)", "achieved": achieved,
                      "peak": peaks["bf16"], "unit": "TFLOP/s", "frac": achieved / peaks["bf16"],
                      "traffic": traffic, "launch_ms": main_ms,
                      "peak_note": f"{peaks['src']} dense BF16 burst (cuBLAS); sustained {peaks['bf16_sustained']}"},
-        "e2e": {"value": world * flops_b / (r["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": flops_b / (r["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms": r["e2e_ms"],
                 "what": ("attnqat_bwd_host with pinned host inputs (dO, Q, K, V, O', LSE) and outputs (dQ, dK, dV); "
                          f"{E2E_CHUNKS} head groups, copies overlapping the kernels")},
