@@ -35,6 +35,7 @@ from __future__ import annotations
 
 import numpy as np
 
+from .fp8 import fp8_round
 from .nvfp4 import fake_nvfp4, fl32
 
 ROW_BLOCK = 256
@@ -223,7 +224,20 @@ def infer_fwd(q, k, v, scale, causal=False, quantize=True):
 R2_BLOCK_N = 128
 
 
-def r2_rows(qh, kh, vh, scale, causal, r0, r1, block_n=R2_BLOCK_N, quantize=True):
+R2_P_FORMATS = ("nvfp4", "e5m2", "e4m3")
+
+
+def _r2_p_hat(p, p_format, quantize):
+    """P^ of one key tile's unnormalised P: fake_nvfp4 in 16-key groups, or the
+    FP8 cast of the FP8-P variant (both on the FP32 value of P)."""
+    if not quantize:
+        return np.asarray(p, np.float64)
+    if p_format == "nvfp4":
+        return p_hat(p, True)
+    return fp8_round(fl32(p), p_format)
+
+
+def r2_rows(qh, kh, vh, scale, causal, r0, r1, block_n=R2_BLOCK_N, quantize=True, p_format="nvfp4"):
     """Recipe R2, the one-pass forward, for query rows [r0, r1) of one head:
     (O, O', LSE).
 
@@ -235,6 +249,8 @@ def r2_rows(qh, kh, vh, scale, causal, r0, r1, block_n=R2_BLOCK_N, quantize=True
         m_j   = max(m_{j-1}, max_k S_jk)          the exact running max
         P_j   = exp(S_j - m_j)                    unnormalised
         P^_j  = fake_nvfp4(fl32(P_j))             groups of 16 keys of the tile
+                (p_format "e5m2" / "e4m3": the FP8 cast fp8(fl32(P_j)) of the
+                FP8-P variant, element by element)
         a_j   = exp(m_{j-1} - m_j)
         l_j   = a_j l_{j-1} + rowsum(P_j)         from the unquantized P
         O'_j  = a_j O'_{j-1} + P_j V^_j
@@ -243,6 +259,8 @@ def r2_rows(qh, kh, vh, scale, causal, r0, r1, block_n=R2_BLOCK_N, quantize=True
     with O = O_n / l_n, O' = O'_n / l_n and LSE = m_n + ln l_n. O' and LSE
     equal the standard forward's, so the backward is the same; only O
     differs, because P^ is formed before normalisation."""
+    if p_format not in R2_P_FORMATS:
+        raise ValueError(f"p_format must be one of {R2_P_FORMATS}")
     s = _logits(qh[r0:r1], kh, scale, causal, r0)
     n, Sk = s.shape[0], s.shape[1]
     m = np.full(n, -np.inf)
@@ -257,15 +275,17 @@ def r2_rows(qh, kh, vh, scale, causal, r0, r1, block_n=R2_BLOCK_N, quantize=True
         a = np.where(np.isfinite(m), np.exp(m - np.where(live, m_new, 0.0)), 0.0)
         p = np.where(live[:, None], np.exp(st - np.where(live, m_new, 0.0)[:, None]), 0.0)
         l = a * l + p.sum(axis=1)
-        acc = a[:, None] * acc + p_hat(p, quantize) @ vh[c0:c1]
+        acc = a[:, None] * acc + _r2_p_hat(p, p_format, quantize) @ vh[c0:c1]
         acc_hp = a[:, None] * acc_hp + p @ vh[c0:c1]
         m = m_new
     return acc / l[:, None], acc_hp / l[:, None], m + np.log(l)
 
 
-def r2_fwd(q, k, v, scale, causal=False, block_n=R2_BLOCK_N, quantize=True):
+def r2_fwd(q, k, v, scale, causal=False, block_n=R2_BLOCK_N, quantize=True, p_format="nvfp4"):
     """Recipe R2 on BHSD float64 arrays: (O, O', LSE) (see r2_rows); Q^, K^,
-    V^ are fake_nvfp4 of Q, K, V as in the standard forward."""
+    V^ are fake_nvfp4 of Q, K, V as in the standard forward; ``p_format``
+    picks the probability quantizer ("nvfp4", or "e5m2" / "e4m3" for the
+    FP8-P variant)."""
     q, k, v = (np.asarray(t, np.float64) for t in (q, k, v))
     if causal and q.shape[2] != k.shape[2]:
         raise ValueError("causal attention needs Sq == Sk")
@@ -279,7 +299,7 @@ def r2_fwd(q, k, v, scale, causal=False, block_n=R2_BLOCK_N, quantize=True):
             for r0 in range(0, Sq, ROW_BLOCK):
                 r1 = min(Sq, r0 + ROW_BLOCK)
                 o[b, h, r0:r1], o_hp[b, h, r0:r1], lse[b, h, r0:r1] = r2_rows(
-                    qh[b, h], kh[b, h], vh[b, h], scale, causal, r0, r1, block_n, quantize)
+                    qh[b, h], kh[b, h], vh[b, h], scale, causal, r0, r1, block_n, quantize, p_format)
     return o, o_hp, lse
 
 

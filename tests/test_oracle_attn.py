@@ -337,3 +337,101 @@ def test_r2_matches_brute_force(Sq, causal):
     np.testing.assert_allclose(o[0, 0], bo, rtol=1e-9, atol=1e-12)
     np.testing.assert_allclose(o_hp[0, 0], bohp, rtol=1e-9, atol=1e-12)
     np.testing.assert_allclose(lse[0, 0], bl, rtol=1e-12)
+
+
+# ------------------------------------------------------------------ recipe R2, FP8-P variant
+def _fp8_golden_rows():
+    path = os.path.join(os.path.dirname(__file__), "golden", "r2_fp8_worked.txt")
+    rows = []
+    for line in open(path):
+        if not line.strip() or line.startswith("#"):
+            continue
+        tag, fmt, bn, logits, c = (f.strip() for f in line.split("|"))
+
+        def vals(txt):
+            out = []
+            for tok in txt.split(","):
+                tok = tok.strip()
+                rep = 1
+                if "*" in tok and tok.rsplit("*", 1)[1].isdigit():
+                    tok, rep = tok.rsplit("*", 1)
+                    rep = int(rep)
+                out += [float(eval(tok, {"__builtins__": {}}, {"ln": math.log}))] * rep
+            return np.array(out)
+        rows.append((tag, fmt, int(bn), vals(logits), vals(c)))
+    return rows
+
+
+@pytest.mark.parametrize("case", _fp8_golden_rows(), ids=lambda c: c[0])
+def test_r2_fp8_worked_examples(case):
+    """Hand-derived FP8-P outputs (tests/golden/r2_fp8_worked.txt): one query
+    row with given logits (Q^ = e_0, K^_j = S_j e_0, scale 1), V^ = identity."""
+    _, fmt, bn, logits, c = case
+    Sk = len(logits)
+    qh = np.zeros((1, 16)); qh[0, 0] = 1.0
+    kh = np.zeros((Sk, 16)); kh[:, 0] = logits
+    vh = np.eye(Sk)
+    o, o_hp, lse = attn.r2_rows(qh, kh, vh, 1.0, False, 0, 1, block_n=bn, p_format=fmt)
+    np.testing.assert_allclose(o[0], c, rtol=1e-12, atol=1e-12)
+    p = np.exp(logits - logits.max())
+    np.testing.assert_allclose(o_hp[0], p / p.sum(), rtol=1e-12)
+
+
+def _brute_fp8(x, fmt):
+    """Nearest FP8 value by enumeration of the format's codes, ties to even."""
+    from test_oracle_fp8 import brute
+    return float(brute([x], fmt)[0])
+
+
+def _brute_r2_fp8(q, k, v, scale, causal, bn, fmt):
+    """Scalar pure-Python FP8-P recipe R2 on one head (enumeration quantizers)."""
+    Sq, D, Sk = len(q), len(q[0]), len(k)
+    quant = lambda row: sum((list(brute_group(row[g:g + 16])) for g in range(0, len(row), 16)), [])
+    qh, kh, vh = [quant(r) for r in q], [quant(r) for r in k], [quant(r) for r in v]
+    O, Ohp, L = [], [], []
+    for i in range(Sq):
+        m, l = -math.inf, 0.0
+        acc, acc_hp = [0.0] * D, [0.0] * D
+        for c0 in range(0, Sk, bn):
+            keys = range(c0, min(Sk, c0 + bn))
+            s = [scale * sum(qh[i][d] * kh[j][d] for d in range(D)) if not (causal and j > i) else -math.inf
+                 for j in keys]
+            m_new = max([m] + s)
+            a = math.exp(m - m_new) if m > -math.inf else 0.0
+            p = [math.exp(x - m_new) if x > -math.inf else 0.0 for x in s]
+            ph = [_brute_fp8(float(np.float32(x)), fmt) for x in p]
+            l = a * l + sum(p)
+            acc = [a * acc[d] + sum(ph[t] * vh[j][d] for t, j in enumerate(keys)) for d in range(D)]
+            acc_hp = [a * acc_hp[d] + sum(p[t] * vh[j][d] for t, j in enumerate(keys)) for d in range(D)]
+            m = m_new
+        O.append([x / l for x in acc]), Ohp.append([x / l for x in acc_hp]), L.append(m + math.log(l))
+    return np.array(O), np.array(Ohp), np.array(L)
+
+
+@pytest.mark.parametrize("fmt", ["e5m2", "e4m3"])
+@pytest.mark.parametrize("Sq,causal", [(5, False), (36, True)])
+def test_r2_fp8_matches_brute_force(Sq, causal, fmt):
+    q, k, v, _ = _inputs(1, 1, Sq, 36, 16, 34, gain=3.0)
+    bo, bohp, bl = _brute_r2_fp8(q[0, 0].tolist(), k[0, 0].tolist(), v[0, 0].tolist(), 0.25, causal, 16, fmt)
+    o, o_hp, lse = attn.r2_fwd(q, k, v, 0.25, causal, block_n=16, p_format=fmt)
+    np.testing.assert_allclose(o[0, 0], bo, rtol=1e-9, atol=1e-12)
+    np.testing.assert_allclose(o_hp[0, 0], bohp, rtol=1e-9, atol=1e-12)
+    np.testing.assert_allclose(lse[0, 0], bl, rtol=1e-12)
+
+
+@pytest.mark.parametrize("fmt", ["e5m2", "e4m3"])
+def test_r2_fp8_identity_and_auxiliary_outputs(fmt):
+    """With identity quantizers every P format is textbook attention; O' and
+    LSE do not depend on the P format; O does, and the FP8 O lies closer to
+    O' than the NVFP4 one (finer probability grid)."""
+    q, k, v, _ = _inputs(1, 2, 45, 45, 16, 35)
+    o, _, _ = attn.r2_fwd(q, k, v, 0.3, True, block_n=16, quantize=False, p_format=fmt)
+    ref = torch.nn.functional.scaled_dot_product_attention(torch.tensor(q), torch.tensor(k), torch.tensor(v),
+                                                           is_causal=True, scale=0.3).numpy()
+    np.testing.assert_allclose(o, ref, rtol=1e-12, atol=1e-12)
+    q, k, v, _ = _inputs(1, 2, 70, 70, 32, 36, gain=2.0)
+    o4, ohp4, lse4 = attn.r2_fwd(q, k, v, 0.2, False, block_n=32)
+    o8, ohp8, lse8 = attn.r2_fwd(q, k, v, 0.2, False, block_n=32, p_format=fmt)
+    np.testing.assert_allclose(ohp8, ohp4, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(lse8, lse4, rtol=1e-14)
+    assert np.linalg.norm(o8 - ohp8) < np.linalg.norm(o4 - ohp4)
