@@ -223,11 +223,17 @@ def run_ours(args, w, rank, world, local_rank, heads=None):
     sp = stream.cuda_stream
     P = lambda a: a.data_ptr()  # noqa: E731
 
-    fwd_main = lib.attnqat_fwd_main_r2 if args.recipe == "r2" else lib.attnqat_fwd_main
+    # the forward is the one API call a user makes: attnqat_fwd (quantize, then
+    # the two passes) or, in recipe R2, attnqat_fwd_r2_p with its P format
+    fmt = attnqat.P_FORMATS[args.recipe[3:] if args.recipe.startswith("r2-") else "nvfp4"]
 
     def fwd():
-        attnqat.check(lib.attnqat_quantize_qkv(pp, P(t["q"]), P(t["k"]), P(t["v"]), P(ws_f), ws_f.numel(), sp), "q")
-        attnqat.check(fwd_main(pp, P(o), P(o_hp), P(lse), P(ws_f), ws_f.numel(), sp), "fwd")
+        if args.recipe == "standard":
+            attnqat.check(lib.attnqat_fwd(pp, P(t["q"]), P(t["k"]), P(t["v"]), P(o), P(o_hp), P(lse), P(ws_f),
+                                          ws_f.numel(), sp), "fwd")
+        else:
+            attnqat.check(lib.attnqat_fwd_r2_p(pp, P(t["q"]), P(t["k"]), P(t["v"]), P(o), P(o_hp), P(lse), fmt,
+                                               P(ws_f), ws_f.numel(), sp), "fwd r2")
 
     def bwd(ev=None):
         attnqat.check(lib.attnqat_bwd_preprocess(pp, P(t["do"]), P(t["q"]), P(t["k"]), P(t["v"]), P(o_hp),
@@ -508,9 +514,10 @@ def main():
     ap.add_argument("--shard", default="none", choices=["none", "heads"],
                     help="with --gpus N: none = every rank runs the whole workload (weak scaling); heads = the "
                          "ranks split its B*H heads into contiguous slices (strong scaling)")
-    ap.add_argument("--recipe", default="standard", choices=["standard", "r2"],
+    ap.add_argument("--recipe", default="standard", choices=["standard", "r2", "r2-e5m2", "r2-e4m3"],
                     help="forward recipe of the QAT step: standard (two passes, P^ of the normalised P) or r2 "
-                         "(one pass, P^ of each key tile's unnormalised P)")
+                         "(one pass, P^ of each key tile's unnormalised P: NVFP4, or the FP8-P variant in E5M2 / "
+                         "E4M3)")
     args = ap.parse_args()
     w = synth.workload(args.workload) if args.seq is None else synth.workload(args.workload, Sq=args.seq,
                                                                                Sk=args.seq)

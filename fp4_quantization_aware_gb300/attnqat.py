@@ -19,6 +19,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libattnqat.so")
 
 ATTNQAT_OK = 0
+# probability quantizers of recipe R2 (attnqat_p_format)
+P_FORMATS = {"nvfp4": 0, "e5m2": 1, "e4m3": 2}
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "misaligned", 4: "workspace", 5: "cuda",
           6: "timeout"}
 
@@ -58,6 +60,7 @@ SIGNATURES = {
     "attnqat_bwd_host": (_S, [_PP, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int, _P, ctypes.c_size_t, _P]),
     "attnqat_device_status": (_S, [ctypes.c_int]),
     "attnqat_selftest_wait_timeout": (_S, [ctypes.c_uint64, _P]),
+    "attnqat_selftest_set_wait_limit": (_S, [ctypes.c_uint64]),
     "attnqat_selftest_quotient": (_S, [_P, _P]),
     "attnqat_selftest_scale": (_S, [_P, _P]),
     "attnqat_nvfp4_pack": (_S, [_P, _P, _P, ctypes.c_int64, ctypes.c_int64, _P]),
@@ -66,6 +69,8 @@ SIGNATURES = {
     "attnqat_infer_fwd": (_S, [_PP, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "attnqat_fwd_r2": (_S, [_PP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "attnqat_fwd_main_r2": (_S, [_PP, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "attnqat_fwd_r2_p": (_S, [_PP, _P, _P, _P, _P, _P, _P, ctypes.c_int, _P, ctypes.c_size_t, _P]),
+    "attnqat_fwd_main_r2_p": (_S, [_PP, _P, _P, _P, ctypes.c_int, _P, ctypes.c_size_t, _P]),
 }
 
 _lib = None
@@ -163,10 +168,11 @@ def fwd(q, k, v, causal=False, scale=None, ws=None, out=None, stream=None):
     return o, o_hp, lse
 
 
-def fwd_r2(q, k, v, causal=False, scale=None, ws=None, out=None, stream=None):
+def fwd_r2(q, k, v, causal=False, scale=None, ws=None, out=None, stream=None, p_format="nvfp4"):
     """Forward in recipe R2 (each key tile's P quantized before normalisation):
     returns (O, O', LSE) for BHSD BF16 CUDA tensors; O' and LSE are those of
-    ``fwd``, so ``bwd`` applies unchanged."""
+    ``fwd``, so ``bwd`` applies unchanged. ``p_format``: "nvfp4" (fake_nvfp4
+    of 16-key groups), or "e5m2" / "e4m3" for the FP8-P variant."""
     import torch
     _bf16_contig(q, k, v)
     p = _problem_of(q, k, causal, scale)
@@ -181,8 +187,8 @@ def fwd_r2(q, k, v, causal=False, scale=None, ws=None, out=None, stream=None):
         lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
     else:
         o, o_hp, lse = out
-    check(lib.attnqat_fwd_r2(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(o_hp), _ptr(lse), _ptr(ws),
-                             ws.numel(), _stream(stream)), "attnqat_fwd_r2")
+    check(lib.attnqat_fwd_r2_p(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(o_hp), _ptr(lse),
+                               P_FORMATS[p_format], _ptr(ws), ws.numel(), _stream(stream)), "attnqat_fwd_r2_p")
     return o, o_hp, lse
 
 

@@ -6,6 +6,7 @@
 #include <cstring>
 #include <initializer_list>
 
+#include <atomic>
 #include <mutex>
 
 #include "../../include/attnqat.h"
@@ -197,6 +198,9 @@ cudaError_t set_smem(const void* kernel, int bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
+std::atomic<uint64_t> g_wait_limit_ns{kWaitTimeoutNs};
+uint64_t wait_timeout_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+
 }  // namespace attnqat
 
 using namespace attnqat;
@@ -286,33 +290,58 @@ attnqat_status attnqat_fwd(const attnqat_problem* p, const void* q, const void* 
   ATTNQAT_TRY(check_problem(p));
   ATTNQAT_TRY(check_ptrs({q, k, v, o, o_hp, lse}));
   ATTNQAT_TRY(check_ws(ws, ws_bytes, layout(*p, false).total));
-  ATTNQAT_TRY(attnqat_quantize_qkv(p, q, k, v, ws, ws_bytes, stream));
+  const WsLayout w = layout(*p, false);
+  if (!w.packed) {
+    ATTNQAT_TRY(attnqat_quantize_qkv(p, q, k, v, ws, ws_bytes, stream));
+    return attnqat_fwd_main(p, o, o_hp, lse, ws, ws_bytes, stream);
+  }
+  // D = 128: the forward kernel reads Q and K only in their NVFP4 encoding,
+  // so the BF16 Q^, K^ are not written (V^ is: the PV MMAs read it)
+  ATTNQAT_CUDA(launch_prep(to_problem(*p), static_cast<const bf16*>(q), static_cast<const bf16*>(k),
+                           static_cast<const bf16*>(v), nullptr, nullptr, nullptr, nullptr, at<bf16>(ws, w.vh),
+                           nullptr, nullptr, nullptr, 0, at<uint8_t>(ws, w.q4), at<uint8_t>(ws, w.qsf),
+                           at<uint8_t>(ws, w.k4), at<uint8_t>(ws, w.ksf), static_cast<cudaStream_t>(stream)),
+               "fwd quantize");
   return attnqat_fwd_main(p, o, o_hp, lse, ws, ws_bytes, stream);
 }
 
-attnqat_status attnqat_fwd_main_r2(const attnqat_problem* p, void* o, void* o_hp, float* lse, void* ws,
-                                   size_t ws_bytes, void* stream) {
+attnqat_status attnqat_fwd_main_r2_p(const attnqat_problem* p, void* o, void* o_hp, float* lse, int p_format,
+                                     void* ws, size_t ws_bytes, void* stream) {
   ATTNQAT_TRY(check_problem(p));
   ATTNQAT_TRY(check_ptrs({o, o_hp, lse}));
+  if (p_format != ATTNQAT_P_NVFP4 && p_format != ATTNQAT_P_FP8_E5M2 && p_format != ATTNQAT_P_FP8_E4M3)
+    return fail(ATTNQAT_ERR_INVALID_ARG, "p_format must be ATTNQAT_P_NVFP4, ATTNQAT_P_FP8_E5M2 or ATTNQAT_P_FP8_E4M3");
   const WsLayout w = layout(*p, false);
   ATTNQAT_TRY(check_ws(ws, ws_bytes, w.total));
   attnqat_status st = ATTNQAT_OK;
   uint32_t* err = device_error_word(&st);
   if (!err) return st;
   ATTNQAT_CUDA(launch_fwd_r2(to_problem(*p), at<bf16>(ws, w.qh), at<bf16>(ws, w.kh), at<bf16>(ws, w.vh),
-                             static_cast<bf16*>(o), static_cast<bf16*>(o_hp), lse, err,
+                             static_cast<bf16*>(o), static_cast<bf16*>(o_hp), lse, p_format, err,
                              static_cast<cudaStream_t>(stream)),
                "fwd_main_r2");
   return ATTNQAT_OK;
 }
 
-attnqat_status attnqat_fwd_r2(const attnqat_problem* p, const void* q, const void* k, const void* v, void* o,
-                              void* o_hp, float* lse, void* ws, size_t ws_bytes, void* stream) {
+attnqat_status attnqat_fwd_main_r2(const attnqat_problem* p, void* o, void* o_hp, float* lse, void* ws,
+                                   size_t ws_bytes, void* stream) {
+  return attnqat_fwd_main_r2_p(p, o, o_hp, lse, ATTNQAT_P_NVFP4, ws, ws_bytes, stream);
+}
+
+attnqat_status attnqat_fwd_r2_p(const attnqat_problem* p, const void* q, const void* k, const void* v, void* o,
+                                void* o_hp, float* lse, int p_format, void* ws, size_t ws_bytes, void* stream) {
   ATTNQAT_TRY(check_problem(p));
   ATTNQAT_TRY(check_ptrs({q, k, v, o, o_hp, lse}));
+  if (p_format != ATTNQAT_P_NVFP4 && p_format != ATTNQAT_P_FP8_E5M2 && p_format != ATTNQAT_P_FP8_E4M3)
+    return fail(ATTNQAT_ERR_INVALID_ARG, "p_format must be ATTNQAT_P_NVFP4, ATTNQAT_P_FP8_E5M2 or ATTNQAT_P_FP8_E4M3");
   ATTNQAT_TRY(check_ws(ws, ws_bytes, layout(*p, false).total));
   ATTNQAT_TRY(attnqat_quantize_qkv(p, q, k, v, ws, ws_bytes, stream));
-  return attnqat_fwd_main_r2(p, o, o_hp, lse, ws, ws_bytes, stream);
+  return attnqat_fwd_main_r2_p(p, o, o_hp, lse, p_format, ws, ws_bytes, stream);
+}
+
+attnqat_status attnqat_fwd_r2(const attnqat_problem* p, const void* q, const void* k, const void* v, void* o,
+                              void* o_hp, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  return attnqat_fwd_r2_p(p, q, k, v, o, o_hp, lse, ATTNQAT_P_NVFP4, ws, ws_bytes, stream);
 }
 
 attnqat_status attnqat_bwd_preprocess(const attnqat_problem* p, const void* dout, const void* q, const void* k,
@@ -469,6 +498,12 @@ attnqat_status attnqat_selftest_quotient(unsigned long long* out, void* stream) 
 attnqat_status attnqat_selftest_scale(unsigned long long* out, void* stream) {
   ATTNQAT_TRY(check_ptrs({out}));
   ATTNQAT_CUDA(launch_scale_selftest(out, static_cast<cudaStream_t>(stream)), "selftest_scale");
+  return ATTNQAT_OK;
+}
+
+attnqat_status attnqat_selftest_set_wait_limit(uint64_t timeout_ns) {
+  if (timeout_ns > 10000000000ull) return fail(ATTNQAT_ERR_INVALID_ARG, "wait limit above 10 s");
+  attnqat::g_wait_limit_ns.store(timeout_ns, std::memory_order_relaxed);
   return ATTNQAT_OK;
 }
 

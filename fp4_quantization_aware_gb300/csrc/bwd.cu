@@ -886,7 +886,7 @@ cudaError_t launch_bwd(const Problem& p, const bf16* qh, const bf16* kh, const b
   a.causal = p.causal ? 1 : 0;
   a.scale = p.scale, a.c2 = p.scale * kLog2e;
   a.q_sf = qsf, a.k_sf = ksf;
-  a.err = err, a.timeout_ns = kWaitTimeoutNs;
+  a.err = err, a.timeout_ns = wait_timeout_ns();
   const BwdSplit plan = bwd_split_plan(p, device_sm_count());
   a.n_full = static_cast<int>(plan.n_full);
   a.split_acc = split_acc, a.split_cnt = split_cnt;

@@ -560,7 +560,7 @@ cudaError_t launch_fwd(const Problem& p, const bf16* qh, const bf16* kh, const b
   a.n_ktiles = static_cast<int>((p.Sk + kBlockN - 1) / kBlockN);
   a.causal = p.causal ? 1 : 0;
   a.c2 = p.scale * kLog2e;
-  a.err = err, a.timeout_ns = kWaitTimeoutNs;
+  a.err = err, a.timeout_ns = wait_timeout_ns();
   const dim3 grid(static_cast<unsigned>(a.n_qtiles), static_cast<unsigned>(bh));
   if (fp4) {
     cudaError_t e = set_smem(reinterpret_cast<const void*>(&fwd_kernel<128>), FwdLayout<128>::kAlloc);

@@ -10,6 +10,10 @@
 //   l    = rowsum of exp(S - m), O' = P V^ / l, LSE  as in the standard forward
 //   O    = sum_j exp(m_j - m) P^_j V^_j / l
 // (O' and LSE equal the standard recipe's, so the backward is unchanged.)
+// The FP8-P variant (the branch that review is about) replaces fake_nvfp4 by
+// an FP8 cast of each element of P_j, round to nearest even: E5M2 (Triton's
+// tl.float8e5, which the review names) or E4M3. The kernel is a template on
+// this P format (kPNvfp4, kPE5M2, kPE4M3).
 //
 // The accumulators use a reference max m_ref that moves only when the running
 // max exceeds it by more than kRescaleLog2 (then O', O and l are rescaled), so
@@ -37,6 +41,41 @@ constexpr int kThreadsR2 = 10 * 32;
 constexpr int kWarpTmaR2 = 8;
 constexpr int kWarpMmaR2 = 9;
 constexpr float kRescaleLog2R2 = 8.0f;
+
+// P^ of one tile for the P formats: 16 unnormalised probabilities (>= 0,
+// <= 1) of one thread, times g (the scale into the accumulators' reference),
+// as 8 BF16 pairs. NVFP4: fake_nvfp4 of the group. FP8: the hardware
+// conversion cvt.rn.satfinite.{e5m2x2,e4m3x2}.f32 (round to nearest even)
+// and back to FP16, which holds both formats exactly.
+template <int PF>
+__device__ __forceinline__ void p_hat_16(const float* x, float g, uint32_t* out8) {
+  if constexpr (PF == kPNvfp4) {
+    fake_nvfp4_16_pack_nonneg<true>(x, g, out8);
+  } else {
+    const float2 g2 = make_float2(g, g);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      uint32_t h2;
+      if constexpr (PF == kPE5M2) {
+        asm("{\n\t.reg .b16 t;\n\t"
+            "cvt.rn.satfinite.e5m2x2.f32 t, %1, %2;\n\t"
+            "cvt.rn.f16x2.e5m2x2 %0, t;\n\t}"
+            : "=r"(h2)
+            : "f"(x[2 * k + 1]), "f"(x[2 * k]));
+      } else {
+        asm("{\n\t.reg .b16 t;\n\t"
+            "cvt.rn.satfinite.e4m3x2.f32 t, %1, %2;\n\t"
+            "cvt.rn.f16x2.e4m3x2 %0, t;\n\t}"
+            : "=r"(h2)
+            : "f"(x[2 * k + 1]), "f"(x[2 * k]));
+      }
+      const float2 y = fmul2(make_float2(__half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu))),
+                                         __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)))),
+                             g2);
+      out8[k] = pack_bf16x2(y.x, y.y);
+    }
+  }
+}
 
 template <int D>
 struct R2Layout {
@@ -82,7 +121,7 @@ struct R2Args {
   uint64_t timeout_ns;
 };
 
-template <int D>
+template <int D, int PF>
 __global__ void __launch_bounds__(kThreadsR2, 1)
     fwd_r2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const R2Args a) {
@@ -316,7 +355,7 @@ __global__ void __launch_bounds__(kThreadsR2, 1)
       }
       uint32_t phw[32];
 #pragma unroll
-      for (int g = 0; g < 4; ++g) fake_nvfp4_16_pack_nonneg<true>(pq + 16 * g, G, phw + 8 * g);
+      for (int g = 0; g < 4; ++g) p_hat_16<PF>(pq + 16 * g, G, phw + 8 * g);
       tmem_st32(scol, pw);                                   // over this warp's own S columns
       tmem_st32(scol + 32, phw);
       tc_fence_before();
@@ -354,10 +393,30 @@ __global__ void __launch_bounds__(kThreadsR2, 1)
   }
 }
 
+template <int D, int PF>
+cudaError_t launch_r2(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const R2Args& a,
+                      dim3 grid, cudaStream_t st) {
+  cudaError_t e = set_smem(reinterpret_cast<const void*>(&fwd_r2_kernel<D, PF>), R2Layout<D>::kAlloc);
+  if (e != cudaSuccess) return e;
+  fwd_r2_kernel<D, PF><<<grid, kThreadsR2, R2Layout<D>::kAlloc, st>>>(tq, tk, tv, a);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_r2_fmt(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const R2Args& a,
+                          dim3 grid, int p_format, cudaStream_t st) {
+  switch (p_format) {
+    case kPNvfp4: return launch_r2<D, kPNvfp4>(tq, tk, tv, a, grid, st);
+    case kPE5M2: return launch_r2<D, kPE5M2>(tq, tk, tv, a, grid, st);
+    case kPE4M3: return launch_r2<D, kPE4M3>(tq, tk, tv, a, grid, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_fwd_r2(const Problem& p, const bf16* qh, const bf16* kh, const bf16* vh, bf16* o, bf16* o_hp,
-                          float* lse, uint32_t* err, cudaStream_t st) {
+                          float* lse, int p_format, uint32_t* err, cudaStream_t st) {
   CUtensorMap tq, tk, tv;
   const uint64_t bh = p.bh();
   if (!make_tile_map(&tq, qh, false, p.D, p.Sq, bh, 64, 128) || !make_tile_map(&tk, kh, false, p.D, p.Sk, bh, 64, 128) ||
@@ -370,18 +429,10 @@ cudaError_t launch_fwd_r2(const Problem& p, const bf16* qh, const bf16* kh, cons
   a.n_ktiles = static_cast<int>((p.Sk + kBlockN - 1) / kBlockN);
   a.causal = p.causal ? 1 : 0;
   a.c2 = p.scale * kLog2e;
-  a.err = err, a.timeout_ns = kWaitTimeoutNs;
+  a.err = err, a.timeout_ns = wait_timeout_ns();
   const dim3 grid(static_cast<unsigned>(a.n_qtiles), static_cast<unsigned>(bh));
-  if (p.D == 128) {
-    cudaError_t e = set_smem(reinterpret_cast<const void*>(&fwd_r2_kernel<128>), R2Layout<128>::kAlloc);
-    if (e != cudaSuccess) return e;
-    fwd_r2_kernel<128><<<grid, kThreadsR2, R2Layout<128>::kAlloc, st>>>(tq, tk, tv, a);
-  } else {
-    cudaError_t e = set_smem(reinterpret_cast<const void*>(&fwd_r2_kernel<64>), R2Layout<64>::kAlloc);
-    if (e != cudaSuccess) return e;
-    fwd_r2_kernel<64><<<grid, kThreadsR2, R2Layout<64>::kAlloc, st>>>(tq, tk, tv, a);
-  }
-  return cudaGetLastError();
+  return p.D == 128 ? launch_r2_fmt<128>(tq, tk, tv, a, grid, p_format, st)
+                    : launch_r2_fmt<64>(tq, tk, tv, a, grid, p_format, st);
 }
 
 }  // namespace attnqat

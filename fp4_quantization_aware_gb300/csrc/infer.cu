@@ -383,7 +383,7 @@ cudaError_t launch_infer(const Problem& p, const uint8_t* q_fp4, const uint8_t* 
   a.n_ktiles = static_cast<int>((p.Sk + kBlockN - 1) / kBlockN);
   a.causal = p.causal ? 1 : 0;
   a.c2 = p.scale * kLog2e;
-  a.err = err, a.timeout_ns = kWaitTimeoutNs;
+  a.err = err, a.timeout_ns = wait_timeout_ns();
   cudaError_t e = set_smem(reinterpret_cast<const void*>(&infer_kernel), InfLayout::kAlloc);
   if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>(a.n_qtiles), static_cast<unsigned>(bh));

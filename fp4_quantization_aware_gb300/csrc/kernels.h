@@ -19,8 +19,11 @@ struct Problem {
 constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
 
-// Wait limit of the attention kernels' barrier waits.
+// Default wait limit of the attention kernels' barrier waits.
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+// The limit the next launches use: kWaitTimeoutNs unless a test has set
+// another through attnqat_selftest_set_wait_limit.
+uint64_t wait_timeout_ns();
 
 cudaError_t launch_fake_bf16(const bf16* x, bf16* y, int64_t rows, int64_t cols, cudaStream_t st);
 cudaError_t launch_fake_f32(const float* x, float* y, int64_t rows, int64_t cols, cudaStream_t st);
@@ -63,8 +66,13 @@ inline int64_t split_slot_floats(const Problem& p) { return 2 * 128 * p.D; }
 
 // The forward in recipe R2 (one pass; P^ of each key tile quantized before
 // normalisation) from the quantize step's Q^, K^, V^; same outputs as launch_fwd.
+// Probability formats of recipe R2 (the values of attnqat_p_format).
+constexpr int kPNvfp4 = 0;
+constexpr int kPE5M2 = 1;
+constexpr int kPE4M3 = 2;
+
 cudaError_t launch_fwd_r2(const Problem& p, const bf16* qh, const bf16* kh, const bf16* vh, bf16* o, bf16* o_hp,
-                          float* lse, uint32_t* err, cudaStream_t st);
+                          float* lse, int p_format, uint32_t* err, cudaStream_t st);
 
 cudaError_t launch_bwd(const Problem& p, const bf16* qh, const bf16* kh, const bf16* vh, const bf16* dout,
                        const float* lse, const float* delta, float* dq_acc, bf16* dk, bf16* dv, float* split_acc,

@@ -70,8 +70,15 @@ __device__ __forceinline__ void raise_error(const WaitCtl& c, uint32_t code) {
 
 // Wait for the phase of `bar` with the given parity to complete. Returns false
 // if the CTA is aborting or the wait ran out of time (then the error is set).
+// A limit of 0 gives up at the first poll that finds the phase incomplete (a
+// poll can itself suspend until the phase completes, so short nonzero limits
+// are not a reliable way to make a wait run out).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtl& c) {
   if (mbar_try_wait(bar, parity)) return true;
+  if (c.timeout_ns == 0) {
+    raise_error(c, kDevTimeout);
+    return false;
+  }
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
 #pragma unroll 1
@@ -96,12 +103,17 @@ __device__ __forceinline__ bool mbar_wait_both(uint64_t* b0, uint32_t p0, uint64
   return (r0 || mbar_wait(b0, p0, c)) && (r1 || mbar_wait(b1, p1, c));
 }
 
+// Limit of the teardown waits below. It is fixed, whatever limit the CTA's
+// other waits run under, so a shortened wait limit can never release shared
+// memory or TMEM while one of the CTA's own copies or MMAs is still in flight.
+constexpr uint64_t kDrainTimeoutNs = 2000000000ull;
+
 // Bounded wait that ignores the abort flag: used at teardown to let this CTA's
 // own in-flight copies and MMAs land before shared memory and TMEM are freed.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, const WaitCtl& c) {
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > c.timeout_ns) {
+    if (globaltimer_ns() - t0 > kDrainTimeoutNs) {
       raise_error(c, kDevTimeout);
       return false;
     }

@@ -99,8 +99,10 @@ attnqat_status attnqat_fake_nvfp4_f32(const float* x, float* y, int64_t rows, in
 
 /* Forward. Inputs q, k, v (BF16). Outputs o = fake_nvfp4(P) V^, o_hp = P V^
  * (both BF16, shape of q) and lse (FP32, natural log). Needs a workspace of
- * attnqat_fwd_workspace_bytes(p) bytes, 256-byte aligned. Equivalent to
- * attnqat_quantize_qkv followed by attnqat_fwd_main. */
+ * attnqat_fwd_workspace_bytes(p) bytes, 256-byte aligned. Same outputs as
+ * attnqat_quantize_qkv followed by attnqat_fwd_main; at D = 128 its quantize
+ * step writes only what the forward kernel reads (the NVFP4 Q, K and the
+ * BF16 V^), not the BF16 Q^, K^. */
 attnqat_status attnqat_fwd(const attnqat_problem* p, const void* q, const void* k, const void* v, void* o,
                            void* o_hp, float* lse, void* workspace, size_t workspace_bytes, void* stream);
 
@@ -142,7 +144,8 @@ attnqat_status attnqat_quantize_qkv(const attnqat_problem* p, const void* q, con
                                     void* workspace, size_t workspace_bytes, void* stream);
 
 /* Forward step 2: the attention kernel on the workspace's Q^, K^, V^ (pass 1:
- * LSE; pass 2: P, fake_nvfp4(P), O' and O). */
+ * LSE; pass 2: P, fake_nvfp4(P), O' and O). At D = 128 it reads Q^ and K^ in
+ * their NVFP4 encoding only. */
 attnqat_status attnqat_fwd_main(const attnqat_problem* p, void* o, void* o_hp, float* lse, void* workspace,
                                 size_t workspace_bytes, void* stream);
 
@@ -163,6 +166,26 @@ attnqat_status attnqat_fwd_r2(const attnqat_problem* p, const void* q, const voi
 /* Step 2 of attnqat_fwd_r2, after attnqat_quantize_qkv. */
 attnqat_status attnqat_fwd_main_r2(const attnqat_problem* p, void* o, void* o_hp, float* lse, void* workspace,
                                    size_t workspace_bytes, void* stream);
+
+/* Probability quantizers of recipe R2: NVFP4 (fake_nvfp4 in 16-key groups,
+ * attnqat_fwd_r2), or the FP8-P variant of the same review ("when dtype is
+ * tl.float8e5 (FP8) ..."): every element of a tile's unnormalised P cast to
+ * FP8, round to nearest even, E5M2 (Triton's tl.float8e5, the type the review
+ * names) or E4M3FN. */
+typedef enum { ATTNQAT_P_NVFP4 = 0, ATTNQAT_P_FP8_E5M2 = 1, ATTNQAT_P_FP8_E4M3 = 2 } attnqat_p_format;
+
+/* attnqat_fwd_r2 with the probability quantizer p_format (an
+ * attnqat_p_format; any other value returns ATTNQAT_ERR_INVALID_ARG before
+ * any launch). In the FP8 formats P^_j = fp8(exp(S_j - m_j)) element by
+ * element; l still sums the unquantized P, and O', LSE are unchanged. Same
+ * arguments, workspace and outputs as attnqat_fwd. */
+attnqat_status attnqat_fwd_r2_p(const attnqat_problem* p, const void* q, const void* k, const void* v, void* o,
+                                void* o_hp, float* lse, int p_format, void* workspace, size_t workspace_bytes,
+                                void* stream);
+
+/* Step 2 of attnqat_fwd_r2_p, after attnqat_quantize_qkv. */
+attnqat_status attnqat_fwd_main_r2_p(const attnqat_problem* p, void* o, void* o_hp, float* lse, int p_format,
+                                     void* workspace, size_t workspace_bytes, void* stream);
 
 /* Backward step 1: Q^, K^, V^ (and at D = 128 their NVFP4 encodings),
  * delta = rowsum(O' * dO) into the workspace, the FP32 dQ accumulator and the
@@ -272,6 +295,23 @@ attnqat_status attnqat_selftest_scale(unsigned long long* out, void* stream);
  * device error word and returns. Exercises the bounded-wait path without
  * faulting or hanging the GPU. */
 attnqat_status attnqat_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
+
+/* The default limit, in nanoseconds, of the attention kernels' barrier waits. */
+#define ATTNQAT_DEFAULT_WAIT_LIMIT_NS 2000000000ull
+
+/* Test export: sets the limit, in nanoseconds, of the barrier waits of every
+ * attention kernel launched afterwards by this process (above 10 s returns
+ * ATTNQAT_ERR_INVALID_ARG; ATTNQAT_DEFAULT_WAIT_LIMIT_NS restores the
+ * default). A limit of 0 makes every wait give up at the first poll that
+ * finds its phase incomplete: the kernel's CTAs then record
+ * ATTNQAT_ERR_TIMEOUT in the device error word (attnqat_device_status) and
+ * return, which exercises the abort path of the real kernels. (A poll may
+ * suspend until its phase completes, so a short nonzero limit does not
+ * reliably make a wait run out.) The waits at a CTA's teardown, which let its
+ * own copies and MMAs land before its shared memory and TMEM are released,
+ * keep their 2 s limit. Outputs of an aborted call are undefined. Not for
+ * use concurrently with other calls. */
+attnqat_status attnqat_selftest_set_wait_limit(uint64_t timeout_ns);
 
 #ifdef __cplusplus
 }

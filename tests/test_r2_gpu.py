@@ -1,6 +1,6 @@
 """Recipe R2 (one-pass forward, each key tile's P fake-quantized before
 normalisation) on the GPU against oracle.r2_fwd with 128-key tiles, the
-kernel's tile size. O, O': rel-Frobenius <= 1e-2 and cosine >= 0.999; LSE:
+kernel's tile size, with NVFP4 P^ and with the FP8-P variant (E5M2, E4M3). O, O': rel-Frobenius <= 1e-2 and cosine >= 0.999; LSE:
 max abs error <= 1e-3. The full-size shapes are checked on sampled row blocks
 of their first and last head, in the launch configuration the bench uses."""
 import numpy as np
@@ -8,7 +8,7 @@ import pytest
 
 import oracle
 from fp4_quantization_aware_gb300 import attnqat, synth
-from parity import LSE_TOL, REL_TOL, COS_TOL, bf16_dev, rel_cos
+from parity import LSE_TOL, REL_TOL, COS_TOL, assert_tiles, bf16_dev, rel_cos
 
 pytestmark = pytest.mark.gpu
 
@@ -36,17 +36,31 @@ def _check(name, got, ref, report):
     rel, cos = rel_cos(got, ref)
     report.append(f"{name}: rel={rel:.2e} cos={cos:.6f}")
     assert rel <= REL_TOL and cos >= COS_TOL, "\n".join(report)
+    assert_tiles(name, got, ref)
+
+
+FP8_CASES = [c for c in CASES if c[2] > 1]
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c)))
 def test_r2_matches_oracle(lib, case):
+    _run_case(case, "nvfp4")
+
+
+@pytest.mark.parametrize("fmt", ["e5m2", "e4m3"])
+@pytest.mark.parametrize("case", FP8_CASES, ids=lambda c: "x".join(map(str, c)))
+def test_r2_fp8_matches_oracle(lib, case, fmt):
+    _run_case(case, fmt)
+
+
+def _run_case(case, fmt):
     import torch
     w, x = _case(*case)
     q, k, v = (bf16_dev(x[n]) for n in ("q", "k", "v"))
-    o, o_hp, lse = attnqat.fwd_r2(q, k, v, causal=w.causal, scale=w.scale)
+    o, o_hp, lse = attnqat.fwd_r2(q, k, v, causal=w.causal, scale=w.scale, p_format=fmt)
     torch.cuda.synchronize()
     assert attnqat.device_status() == 0
-    ro, rohp, rlse = oracle.r2_fwd(x["q"], x["k"], x["v"], w.scale, w.causal, block_n=128)
+    ro, rohp, rlse = oracle.r2_fwd(x["q"], x["k"], x["v"], w.scale, w.causal, block_n=128, p_format=fmt)
     report = []
     _check("O", o.float().cpu().numpy(), ro, report)
     _check("O'", o_hp.float().cpu().numpy(), rohp, report)
@@ -89,13 +103,14 @@ def _blocks(n, size=64):
     return [(0, size), (mid, mid + size), (n - size, n)]
 
 
-@pytest.mark.parametrize("name", ["c2", "c3", "c5"])
-def test_r2_full_size_sampled(lib, name):
+@pytest.mark.parametrize("name,fmt", [("c2", "nvfp4"), ("c3", "nvfp4"), ("c5", "nvfp4"), ("c2", "e5m2"),
+                                      ("c5", "e4m3")])
+def test_r2_full_size_sampled(lib, name, fmt):
     import torch
     w = synth.workload(name)
     x = synth.inputs(w)
     q, k, v = (bf16_dev(x[n]) for n in ("q", "k", "v"))
-    o, o_hp, lse = attnqat.fwd_r2(q, k, v, causal=w.causal, scale=w.scale)
+    o, o_hp, lse = attnqat.fwd_r2(q, k, v, causal=w.causal, scale=w.scale, p_format=fmt)
     torch.cuda.synchronize()
     assert attnqat.device_status() == 0
     go, gohp, glse = (t.float().cpu().numpy() for t in (o, o_hp, lse))
@@ -104,9 +119,35 @@ def test_r2_full_size_sampled(lib, name):
         qh, kh, vh = oracle.hats(x["q"][b, h].astype(np.float64), x["k"][b, h].astype(np.float64),
                                  x["v"][b, h].astype(np.float64))
         for r0, r1 in _blocks(w.Sq):
-            ro, rohp, rl = oracle.r2_rows(qh, kh, vh, w.scale, w.causal, r0, r1)
+            ro, rohp, rl = oracle.r2_rows(qh, kh, vh, w.scale, w.causal, r0, r1, p_format=fmt)
             _check(f"{name} ({b},{h}) O[{r0}:{r1}]", go[b, h, r0:r1], ro, report)
             _check(f"{name} ({b},{h}) O'[{r0}:{r1}]", gohp[b, h, r0:r1], rohp, report)
             err = float(np.max(np.abs(glse[b, h, r0:r1] - rl)))
             assert err <= LSE_TOL, f"{name} ({b},{h}) LSE[{r0}:{r1}] {err:.2e}"
     print("\n".join(report))
+
+
+def test_r2_fp8_is_its_own_recipe(lib):
+    """The FP8 variants keep O' and LSE of the NVFP4 one bit for bit (only P^
+    changes) and their O differs from it, closer to O' (finer grid)."""
+    import torch
+    w, x = _case(1, 2, 512, 512, 128, False, "peaked")
+    q, k, v = (bf16_dev(x[n]) for n in ("q", "k", "v"))
+    o4, ohp4, lse4 = attnqat.fwd_r2(q, k, v, scale=w.scale)
+    for fmt in ("e5m2", "e4m3"):
+        o8, ohp8, lse8 = attnqat.fwd_r2(q, k, v, scale=w.scale, p_format=fmt)
+        torch.cuda.synchronize()
+        assert torch.equal(ohp8, ohp4) and torch.equal(lse8, lse4)
+        d8 = (o8.float() - ohp8.float()).norm().item()
+        d4 = (o4.float() - ohp4.float()).norm().item()
+        assert 0 < d8 < d4, (fmt, d8, d4)
+
+
+def test_r2_rejects_unknown_p_format(lib):
+    import ctypes
+    p = attnqat.problem(1, 1, 128, 128, 128)
+    x = bf16_dev(np.zeros((1, 1, 128, 128), np.float32))
+    ws = attnqat.workspace(lib.attnqat_fwd_workspace_bytes(ctypes.byref(p)), x.device)
+    st = lib.attnqat_fwd_r2_p(ctypes.byref(p), x.data_ptr(), x.data_ptr(), x.data_ptr(), x.data_ptr(), x.data_ptr(),
+                              x.data_ptr(), 7, ws.data_ptr(), ws.numel(), None)
+    assert st == 1
