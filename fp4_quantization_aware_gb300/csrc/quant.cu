@@ -134,22 +134,9 @@ __global__ void __launch_bounds__(kThreads) prep_kernel(PrepArgs a) {
   }
   const bool live = g < a.groups[t];
   if (blockIdx.x * static_cast<int64_t>(kThreads) >= a.groups[t]) return;   // whole block out of range
-  const bool with_delta = t == 0 && a.o_hp != nullptr;
-  // Every load of the thread is issued before any arithmetic, so their
-  // latencies overlap (the kernel is bound by bytes in flight).
-  uint4 src[2], oh[2], dd[2];
+  float f[16];
   if (live) {
-    const uint4* sp = reinterpret_cast<const uint4*>(a.src[t] + g * 16);
-    src[0] = __ldg(sp), src[1] = __ldg(sp + 1);
-    if (with_delta) {
-      const uint4* op = reinterpret_cast<const uint4*>(a.o_hp + g * 16);
-      const uint4* dp = reinterpret_cast<const uint4*>(a.dout + g * 16);
-      oh[0] = __ldg(op), oh[1] = __ldg(op + 1), dd[0] = __ldg(dp), dd[1] = __ldg(dp + 1);
-    }
-  }
-  if (live) {
-    float f[16];
-    unpack8(src[0], f), unpack8(src[1], f + 8);
+    load16(a.src[t] + g * 16, f);
     if (t < 2 && a.packed[t] != nullptr) {   // the same values, NVFP4-encoded
       uint8_t b[8];
       a.scales[t][g] = nvfp4_encode_16(f, b);
@@ -163,12 +150,13 @@ __global__ void __launch_bounds__(kThreads) prep_kernel(PrepArgs a) {
       store16(a.dst[t] + g * 16, f);
     }
   }
-  if (!with_delta) return;
+  if (t != 0 || a.o_hp == nullptr) return;
   // delta = rowsum(O' * dO); every lane of the warp takes part in the shuffles.
   float part = 0.0f;
   if (live) {
     float o[16], d[16];
-    unpack8(oh[0], o), unpack8(oh[1], o + 8), unpack8(dd[0], d), unpack8(dd[1], d + 8);
+    load16(a.o_hp + g * 16, o);
+    load16(a.dout + g * 16, d);
 #pragma unroll
     for (int i = 0; i < 16; ++i) part = fmaf(o[i], d[i], part);
     float4* z = reinterpret_cast<float4*>(a.dq_acc + g * 16);
@@ -180,22 +168,12 @@ __global__ void __launch_bounds__(kThreads) prep_kernel(PrepArgs a) {
   if (live && (g % kGroupsPerRow) == 0) a.delta[g / kGroupsPerRow] = part;
 }
 
-// Each thread converts kConvPerThread float4s a grid's width apart, all loads
-// issued before the stores (bytes in flight bound this kernel); the FP32
-// accumulator is read once, so its loads are marked streaming.
-constexpr int kConvPerThread = 4;
-
 __global__ void __launch_bounds__(kThreads) dq_convert_kernel(const float4* __restrict__ acc, uint2* __restrict__ dq,
                                                               int64_t n4) {
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
-  float4 v[kConvPerThread];
-#pragma unroll
-  for (int u = 0; u < kConvPerThread; ++u)
-    if (i0 + u * stride < n4) v[u] = __ldcs(acc + i0 + u * stride);
-#pragma unroll
-  for (int u = 0; u < kConvPerThread; ++u)
-    if (i0 + u * stride < n4) dq[i0 + u * stride] = make_uint2(pack_bf16x2(v[u].x, v[u].y), pack_bf16x2(v[u].z, v[u].w));
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+  if (i >= n4) return;
+  const float4 v = acc[i];
+  dq[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
 }
 
 // One CTA waits on a barrier that nothing arrives at; the bounded wait gives
@@ -360,9 +338,8 @@ cudaError_t launch_nvfp4_pack(const bf16* x, uint8_t* packed, uint8_t* scales, i
 
 cudaError_t launch_dq_convert(const Problem& p, const float* dq_acc, bf16* dq, cudaStream_t st) {
   const int64_t n4 = p.bh() * p.Sq * p.D / 4;
-  if (n4 == 0) return cudaSuccess;
-  dq_convert_kernel<<<blocks_for((n4 + kConvPerThread - 1) / kConvPerThread), kThreads, 0, st>>>(
-      reinterpret_cast<const float4*>(dq_acc), reinterpret_cast<uint2*>(dq), n4);
+  dq_convert_kernel<<<blocks_for(n4), kThreads, 0, st>>>(reinterpret_cast<const float4*>(dq_acc),
+                                                         reinterpret_cast<uint2*>(dq), n4);
   return cudaGetLastError();
 }
 
