@@ -281,7 +281,7 @@ def run_ours(args, w, rank, world, local_rank, heads=None):
     host_in["o_hp"] = o_hp.cpu().pin_memory()
     host_in["lse"] = lse.cpu().pin_memory()
     host_out = [torch.empty_like(a, device="cpu").pin_memory() for a in (dq, dk, dv)]
-    ws_h = attnqat.workspace(lib.attnqat_bwd_host_workspace_bytes(pp, E2E_CHUNKS), dev)
+    ws_h = attnqat.workspace(lib.attnqat_bwd_host_workspace_bytes(pp, args.e2e_chunks), dev)
     e2e_evs = [(E(), E()) for _ in range(args.steps)]
     for i in range(args.warmup + args.steps):
         flush.zero_()
@@ -289,7 +289,7 @@ def run_ours(args, w, rank, world, local_rank, heads=None):
             e2e_evs[i - args.warmup][0].record(stream)
         attnqat.check(lib.attnqat_bwd_host(pp, P(host_in["do"]), P(host_in["q"]), P(host_in["k"]), P(host_in["v"]),
                                            P(host_in["o_hp"]), P(host_in["lse"]), P(host_out[0]), P(host_out[1]),
-                                           P(host_out[2]), E2E_CHUNKS, P(ws_h), ws_h.numel(), sp), "bwd e2e")
+                                           P(host_out[2]), args.e2e_chunks, P(ws_h), ws_h.numel(), sp), "bwd e2e")
         if i >= args.warmup:
             e2e_evs[i - args.warmup][1].record(stream)
     torch.cuda.synchronize()
@@ -511,6 +511,8 @@ def main():
                     help="qat: the QAT forward+backward step; infer: the NVFP4 inference forward "
                          "(default: infer for ctx32k, qat otherwise)")
     ap.add_argument("--seq", type=int, default=None, help="override Sq = Sk of the workload (smaller captures)")
+    ap.add_argument("--e2e-chunks", type=int, default=E2E_CHUNKS,
+                    help="head groups of the end-to-end (host-buffer) backward")
     ap.add_argument("--shard", default="none", choices=["none", "heads"],
                     help="with --gpus N: none = every rank runs the whole workload (weak scaling); heads = the "
                          "ranks split its B*H heads into contiguous slices (strong scaling)")
@@ -635,7 +637,7 @@ def main():
         "e2e": {"value": flops_b / (r["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms": r["e2e_ms"],
                 "what": ("attnqat_bwd_host with pinned host inputs (dO, Q, K, V, O', LSE) and outputs (dQ, dK, dV); "
-                         f"{E2E_CHUNKS} head groups, copies overlapping the kernels")},
+                         f"{args.e2e_chunks} head groups, copies overlapping the kernels")},
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
     }

@@ -85,7 +85,8 @@ attnqat_status check_problem(const attnqat_problem* p) {
   if (p->is_causal && p->Sq != p->Sk) return fail(ATTNQAT_ERR_UNSUPPORTED, "causal attention needs Sq == Sk");
   if (p->Sq >= (int64_t(1) << 31) - 256 || p->Sk >= (int64_t(1) << 31) - 256)
     return fail(ATTNQAT_ERR_UNSUPPORTED, "sequence length beyond 2^31");
-  if (p->B * p->H > 65535) return fail(ATTNQAT_ERR_UNSUPPORTED, "B*H above 65535");
+  // each factor first, so that the product cannot wrap
+  if (p->B > 65535 || p->H > 65535 || p->B * p->H > 65535) return fail(ATTNQAT_ERR_UNSUPPORTED, "B*H above 65535");
   return ATTNQAT_OK;
 }
 

@@ -6,8 +6,15 @@
 // c - 1 is copied out on the other, so the host<->device transfers overlap
 // the kernels. Two device slots, each holding one group's inputs, outputs and
 // backward workspace, alternate between groups; events order each slot's
-// reuse: the copy-in of group c + 2 waits for the copy-out of group c, which
-// waited for group c's kernels.
+// reuse. The copy-in of group c + 2 waits only for group c's kernels (the
+// last readers of the slot's inputs), so the inputs stream in back to back;
+// group c + 2's kernels wait for the copy-out of group c (the slot's
+// outputs) as well as for their own inputs.
+//
+// The groups hold ceil(B*H / chunks) heads each, except the first and the last
+// ones, which hold half of that: the kernels start after a shorter first copy,
+// and less work is left once the last inputs are in (the copies, not the
+// kernels, bound this call).
 //
 // The copy streams and events are created once per device and shared by all
 // calls, so calls on one device must not run concurrently from several host
@@ -75,6 +82,44 @@ int64_t group_heads(const attnqat_problem& p, int chunks) {
   return (bh + n - 1) / n;
 }
 
+// The first head and the head count of group g of the call's groups (see the
+// file comment): sizes half, full, ..., full, then the remainder, of which a
+// full-size last group is halved.
+struct GroupPlan {
+  int64_t bh, hc, first, n_mid, rest_a, rest_b;   // group sizes: first, n_mid x hc, rest_a, rest_b
+  int64_t groups() const { return 1 + n_mid + (rest_a > 0) + (rest_b > 0); }
+  void group(int64_t g, int64_t& h0, int64_t& nh) const {
+    if (g == 0) { h0 = 0, nh = first; return; }
+    if (g <= n_mid) { h0 = first + (g - 1) * hc, nh = hc; return; }
+    h0 = first + n_mid * hc;
+    if (g == n_mid + 1 && rest_a > 0) { nh = rest_a; return; }
+    h0 += rest_a, nh = rest_b;
+  }
+};
+
+GroupPlan plan_groups(int64_t bh, int64_t hc) {
+  GroupPlan p{bh, hc, 0, 0, 0, 0};
+  p.first = hc > 1 ? (hc + 1) / 2 : 1;
+  if (p.first >= bh) {
+    p.first = bh;
+    return p;
+  }
+  int64_t rest = bh - p.first;
+  p.n_mid = rest / hc;
+  rest -= p.n_mid * hc;
+  if (rest == 0 && p.n_mid > 0 && hc > 1) {   // the last full group becomes two halves
+    --p.n_mid;
+    rest = hc;
+  }
+  if (rest > (hc + 1) / 2 && hc > 1) {
+    p.rest_a = rest - (hc + 1) / 2;
+    p.rest_b = (hc + 1) / 2;
+  } else {
+    p.rest_a = rest;
+  }
+  return p;
+}
+
 attnqat_status streams_for(int dev, CopyStreams** out) {
   std::lock_guard<std::mutex> lock(g_mutex);
   CopyStreams& s = g_streams[dev];
@@ -117,7 +162,9 @@ extern "C" attnqat_status attnqat_bwd_host(const attnqat_problem* p, const void*
       attnqat::set_error_message("attnqat_bwd_host: a host tensor pointer is null");
       return ATTNQAT_ERR_INVALID_ARG;
     }
-  const int64_t bh = p->B * p->H, hc = group_heads(*p, chunks), groups = (bh + hc - 1) / hc;
+  const int64_t bh = p->B * p->H, hc = group_heads(*p, chunks);
+  const GroupPlan plan = plan_groups(bh, hc);
+  const int64_t groups = plan.groups();
   const SlotLayout L = slot_layout(*p, hc);
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
       workspace_bytes < 2 * L.total) {
@@ -158,14 +205,16 @@ extern "C" attnqat_status attnqat_bwd_host(const attnqat_problem* p, const void*
   const size_t out_row[3] = {qrow, krow, krow};
   for (int64_t g = 0; ok && g < groups; ++g) {
     const int s = static_cast<int>(g & 1);
-    const int64_t h0 = g * hc, nh = (bh - h0) < hc ? (bh - h0) : hc;
+    int64_t h0 = 0, nh = 0;
+    plan.group(g, h0, nh);
     uint8_t* base = static_cast<uint8_t*>(workspace) + s * L.total;
-    if (g >= 2) cuda(cudaStreamWaitEvent(S->h2d, S->out[s], 0));   // slot s copied out (group g - 2)
+    if (g >= 2) cuda(cudaStreamWaitEvent(S->h2d, S->done[s], 0));   // slot s's inputs read (group g - 2)
     for (int i = 0; i < 6 && ok; ++i)
       cuda(cudaMemcpyAsync(base + in_off[i], hin[i] + h0 * in_row[i], nh * in_row[i], cudaMemcpyHostToDevice,
                            S->h2d));
     cuda(cudaEventRecord(S->in[s], S->h2d));
     cuda(cudaStreamWaitEvent(cs, S->in[s], 0));
+    if (g >= 2) cuda(cudaStreamWaitEvent(cs, S->out[s], 0));         // slot s's outputs copied out (group g - 2)
     if (!ok) break;
     const attnqat_problem gp = group_problem(*p, nh);
     st = attnqat_bwd(&gp, base + L.dout, base + L.q, base + L.k, base + L.v, base + L.o_hp,

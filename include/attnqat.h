@@ -118,9 +118,13 @@ attnqat_status attnqat_bwd(const attnqat_problem* p, const void* dout, const voi
 /* Backward with every input and output in host memory (page-locked, so that
  * the copies overlap the kernels): the backward of the cuDNN page (Overview),
  * computed by the same kernels as attnqat_bwd on groups of heads. The B*H
- * heads are split into `chunks` contiguous groups (clamped to 1..B*H). While
- * group c runs on `stream`, group c + 1 is copied in and group c - 1 out on
- * two copy streams the library creates once per device. Arguments as for
+ * heads are split into contiguous groups of n = ceil(B*H / chunks) heads
+ * (chunks clamped to 1..B*H), except the first and the last groups, which
+ * hold about n / 2 (the transfers bound this call: a short first group
+ * starts the kernels early, a short last group leaves less after the last
+ * copy in). While group c runs on `stream`, group c + 1 is copied in and
+ * group c - 1 out on two copy streams the library creates once per device.
+ * Arguments as for
  * attnqat_bwd, with dout, q, k, v, o_hp, lse, dq, dk, dv host pointers in the
  * same BHSD layouts. The device workspace of
  * attnqat_bwd_host_workspace_bytes(p, chunks) bytes (256-byte aligned) holds

@@ -54,6 +54,9 @@ def test_check_support(clib):
     assert _support(clib, causal=True, Sq=100, Sk=300) == 2
     assert _support(clib, Sq=0) == 1
     assert _support(clib, B=300, H=300) == 2
+    assert _support(clib, B=1 << 62, H=4) == 2                       # B*H wraps to 0 in 64 bits: still rejected
+    assert _support(clib, B=1, H=65535) == 0 and _support(clib, B=1, H=65536) == 2
+    assert _support(clib, Sq=(1 << 31) - 256, Sk=100) == 2           # sequence lengths past the kernels' int range
     assert _support(clib, scale=float("nan")) == 1
     assert _support(clib, scale=-1.0) == 1
     assert clib.attnqat_check_support(None) == 1
