@@ -117,6 +117,7 @@ struct FwdArgs {
   bf16* o;
   bf16* o_hp;
   float* lse;
+  const float* lse_in;   // not null: pass 1 is skipped, this is the LSE (natural log)
   int Sq, Sk;
   int n_qtiles, n_ktiles;
   int causal;
@@ -143,7 +144,11 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
   const int i = a.causal ? (a.n_qtiles - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
   const int bh = blockIdx.y;
   const int nk = a.causal ? i + 1 : a.n_ktiles;
-  const int nt = 2 * nk;                     // pass 1: t < nk; pass 2: t >= nk
+  // Tiles t of the sequence: pass 1 (t < P1, key tile t), then pass 2 (key
+  // tile t - P1). With lse_in given (D = 128: the paired LSE kernel has
+  // computed the LSE), only pass 2 runs.
+  const int P1 = a.lse_in != nullptr ? 0 : nk;
+  const int nt = P1 + nk;
 
   if (threadIdx.x == 0) {
     B.abort_flag = 0;
@@ -188,7 +193,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
           tma_load_3d(smem + L::kQ + b * kBlockBytes, &tm_q, &B.q_full, b * 64, i * 128, bh);
       }
       for (int t = 0; t < nt; ++t) {
-        const int jt = t < nk ? t : t - nk;
+        const int jt = t < P1 ? t : t - P1;
         const int s = t % L::kStages, use = t / L::kStages;
         if (use >= 1 && !mbar_wait(&B.k_empty[s], (use - 1) & 1, ctl)) break;
         if constexpr (L::kFp4) {                           // NVFP4 K in both passes
@@ -200,8 +205,8 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
             tma_load_3d(smem + L::kK0 + s * L::kTile + b * kBlockBytes, &tm_k, &B.k_full[s], b * 64, jt * 128, bh);
         }
         ++k_uses[s];
-        if (t >= nk) {
-          const int tv = t - nk, sv = tv % L::kStages, vuse = tv / L::kStages;
+        if (t >= P1) {
+          const int tv = t - P1, sv = tv % L::kStages, vuse = tv / L::kStages;
           if (vuse >= 1 && !mbar_wait(&B.v_empty[sv], (vuse - 1) & 1, ctl)) break;
           mbar_arrive_expect_tx(&B.v_full[sv], L::kTile);
           for (int b = 0; b < D / 64; ++b)
@@ -226,7 +231,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       const uint64_t mnmaj = sdesc_sw128(sbase, kBlockBytes, 1024);
       // use index of pass-2 tile t's S buffer among pass-2 tiles (one barrier
       // per buffer, so the softmax warps running ahead cannot alias phases)
-      auto pr_use = [&](int t) { return (t >> 1) - ((nk + 1 - (t & 1)) >> 1); };
+      auto pr_use = [&](int t) { return (t >> 1) - ((P1 + 1 - (t & 1)) >> 1); };
       bool ok = true;
       if (warp == kWarpMmaS) {
         auto issue_s = [&](int t) -> bool {
@@ -238,11 +243,11 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
           // D = 128, pass-2 tiles from the third on: the scale factors are in the
           // previous tile's S buffer, written there once the softmax warps have
           // read that S (they arrive on its s_free in both passes).
-          const bool sf_in_s = L::kFp4 && t >= nk + 2;
-          const bool prev_s = u >= 0 && u < nk;   // exclusive with sf_in_s
+          const bool sf_in_s = L::kFp4 && t >= P1 + 2;
+          const bool prev_s = u >= 0 && u < P1;   // exclusive with sf_in_s
           uint64_t* sbar = prev_s ? &B.s_free[s] : (sf_in_s ? &B.s_free[(t - 1) & 1] : nullptr);
           const uint32_t spar = prev_s ? ((u >> 1) & 1) : (((t - 1) >> 1) & 1);
-          const bool pv_wait = u >= nk;
+          const bool pv_wait = u >= P1;
           const bool kf = mbar_try_wait(&B.k_full[ks_], (t / L::kStages) & 1);
           if (!mbar_wait_both(sbar, spar, pv_wait ? &B.pv_read[s] : nullptr, pv_wait ? (pr_use(u) & 1) : 0u, ctl))
             return false;
@@ -282,13 +287,13 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         const bool is_op = warp == kWarpMmaF;
         // The scale factors of pass 1 and of pass-2 tiles 0, 1 sit in the O'
         // columns: the first O' MMA waits until S of those tiles has completed.
-        if (is_op && L::kFp4 && nk < nt) {
-          const int t0 = nk, t1 = nk + 1;
+        if (is_op && L::kFp4 && P1 < nt) {
+          const int t0 = P1, t1 = P1 + 1;
           ok = mbar_wait_both(&B.s_full[t0 & 1], (t0 >> 1) & 1, t1 < nt ? &B.s_full[t1 & 1] : nullptr,
                               (t1 >> 1) & 1, ctl);
         }
-        for (int t = nk; ok && t < nt; ++t) {
-          const int tv = t - nk, sv = tv % L::kStages;
+        for (int t = P1; ok && t < nt; ++t) {
+          const int tv = t - P1, sv = tv % L::kStages;
           if (!mbar_wait_both(&B.v_full[sv], (tv / L::kStages) & 1, &B.p_ready[t & 1], pr_use(t) & 1, ctl)) break;
           tc_fence_after();
           const uint64_t dv = sdesc_advance(mnmaj, L::kV0 + sv * L::kTile);
@@ -356,16 +361,16 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     float m = -INFINITY, l = 0.0f;
     // K scales written at tile t (those of tile t + 2, up to pass 2's second
     // tile) are loaded one tile ahead, so their latency is off the hand-off
-    auto kt_of = [&](int u) { return u < nk ? u : u - nk; };
+    auto kt_of = [&](int u) { return u < P1 ? u : u - P1; };
     uint32_t sfw[4] = {0u, 0u, 0u, 0u}, sfw_next[4] = {0u, 0u, 0u, 0u};
     if (L::kFp4 && sf_writer && 2 < nt)
       load_scales(a.k_sf, kbase + kt_of(2) * 128, min(128, a.Sk - kt_of(2) * 128), ks, sfw);
-    for (int t = 0; t < nk; ++t) {
+    for (int t = 0; t < P1; ++t) {
       const int s = t & 1;
       const int valid = kend - (t * 128 + static_cast<int>(part) * 32);
       // K scales of tile t + 2 (up to pass 2's second tile, key tile 1)
       const bool more = L::kFp4 && sf_writer && t + 2 < nt;
-      if (L::kFp4 && sf_writer && t + 3 < nt && t + 1 < nk)
+      if (L::kFp4 && sf_writer && t + 3 < nt && t + 1 < P1)
         load_scales(a.k_sf, kbase + kt_of(t + 3) * 128, min(128, a.Sk - kt_of(t + 3) * 128), ks, sfw_next);
       if (!warp_wait(&B.s_full[s], (t >> 1) & 1, ctl)) { ok = false; break; }
       tc_fence_after();
@@ -412,7 +417,9 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     // 0, which forms lse2 = log2 sum 2^(S*c2), stores LSE and hands lse2 back.
     float lse2 = 0.0f;
     float* lse_s = ml + 3 * 256;
-    if (ok && part != 0) {
+    if (P1 == 0) {   // pass 2 only: the LSE of this row from lse_in
+      if (qrow < a.Sq) lse2 = __ldg(a.lse_in + (size_t)bh * a.Sq + qrow) * kLog2e;
+    } else if (ok && part != 0) {
       ml[(part - 1) * 256 + r * 2] = m;
       ml[(part - 1) * 256 + r * 2 + 1] = l;
       mbar_arrive(&B.ml_ready);
@@ -442,8 +449,8 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
     if (L::kFp4 && sf_writer)
       load_scales(a.q_sf, static_cast<int64_t>(bh) * a.Sq + i * 128, min(128, a.Sq - i * 128), ks, sfq);
     uint32_t sfk[4] = {0u, 0u, 0u, 0u};
-    for (int t = nk; ok && t < nt; ++t) {
-      const int s = t & 1, tv = t - nk;
+    for (int t = P1; ok && t < nt; ++t) {
+      const int s = t & 1, tv = t - P1;
       const int valid = kend - (tv * 128 + static_cast<int>(part) * 32);
       // D = 128: parts 1 and 3 put the scale factors of S(t + 1) (pass-2
       // tiles from the third on; K step ks) into S(t)'s buffer, over the P^
@@ -561,9 +568,15 @@ cudaError_t launch_fwd(const Problem& p, const bf16* qh, const bf16* kh, const b
   a.causal = p.causal ? 1 : 0;
   a.c2 = p.scale * kLog2e;
   a.err = err, a.timeout_ns = wait_timeout_ns();
+  a.lse_in = nullptr;
   const dim3 grid(static_cast<unsigned>(a.n_qtiles), static_cast<unsigned>(bh));
   if (fp4) {
-    cudaError_t e = set_smem(reinterpret_cast<const void*>(&fwd_kernel<128>), FwdLayout<128>::kAlloc);
+    // D = 128: pass 1 (the LSE) in the paired kernel of fwd_lse.cu, then pass
+    // 2 here reading it
+    cudaError_t e = launch_fwd_lse(p, q4, qsf, k4, ksf, lse, err, st);
+    if (e != cudaSuccess) return e;
+    a.lse_in = lse;
+    e = set_smem(reinterpret_cast<const void*>(&fwd_kernel<128>), FwdLayout<128>::kAlloc);
     if (e != cudaSuccess) return e;
     fwd_kernel<128><<<grid, kThreadsFwd, FwdLayout<128>::kAlloc, st>>>(tq, tk, tv, tq4, tk4, a);
   } else {

@@ -49,6 +49,11 @@ cudaError_t launch_fwd(const Problem& p, const bf16* qh, const bf16* kh, const b
                        const uint8_t* qsf, const uint8_t* k4, const uint8_t* ksf, bf16* o, bf16* o_hp, float* lse,
                        uint32_t* err, cudaStream_t st);
 
+// Pass 1 of the D = 128 forward: the natural-log LSE of every query row, two
+// query tiles of a head per CTA (S on the block-scaled NVFP4 MMA).
+cudaError_t launch_fwd_lse(const Problem& p, const uint8_t* q4, const uint8_t* qsf, const uint8_t* k4,
+                           const uint8_t* ksf, float* lse, uint32_t* err, cudaStream_t st);
+
 // How the backward shares key tiles between CTAs: the first n_full key tiles
 // (in grid order) get one CTA each, the last n_split two CTAs each (half the
 // query tiles apiece), whose FP32 partial dK, dV meet in a workspace slot.
