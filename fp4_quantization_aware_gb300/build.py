@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libattnqat.so")
-SOURCES = ["api.cu", "quant.cu", "fwd.cu", "fwd_lse.cu", "fwd_r2.cu", "bwd.cu", "infer.cu", "noalloc.cu", "host.cu"]
+SOURCES = ["api.cu", "quant.cu", "fwd.cu", "fwd_lse.cu", "fwd_pv.cu", "fwd_r2.cu", "bwd.cu", "infer.cu", "noalloc.cu", "host.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xcompiler", "-Wall", "-Xcompiler", "-Wno-unused-function"]

@@ -54,6 +54,13 @@ cudaError_t launch_fwd(const Problem& p, const bf16* qh, const bf16* kh, const b
 cudaError_t launch_fwd_lse(const Problem& p, const uint8_t* q4, const uint8_t* qsf, const uint8_t* k4,
                            const uint8_t* ksf, float* lse, uint32_t* err, cudaStream_t st);
 
+// Pass 2 of the D = 128 forward: O' = P V^ and O = fake_nvfp4(P) V^ from pass
+// 1's LSE, one 128-row query tile per CTA over 64-key tiles (S on the
+// block-scaled NVFP4 MMA).
+cudaError_t launch_fwd_pv(const Problem& p, const bf16* vh, const uint8_t* q4, const uint8_t* qsf,
+                          const uint8_t* k4, const uint8_t* ksf, const float* lse, bf16* o, bf16* o_hp,
+                          uint32_t* err, cudaStream_t st);
+
 // How the backward shares key tiles between CTAs: the first n_full key tiles
 // (in grid order) get one CTA each, the last n_split two CTAs each (half the
 // query tiles apiece), whose FP32 partial dK, dV meet in a workspace slot.

@@ -73,12 +73,20 @@ __device__ __forceinline__ void raise_error(const WaitCtl& c, uint32_t code) {
 // A limit of 0 gives up at the first poll that finds the phase incomplete (a
 // poll can itself suspend until the phase completes, so short nonzero limits
 // are not a reliable way to make a wait run out).
+// The first kSpinPolls polls run before the clock is read: reading
+// %globaltimer takes long enough that a phase completing meanwhile would be
+// seen late, and most waits end within those polls.
+constexpr int kSpinPolls = 64;
+
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const WaitCtl& c) {
   if (mbar_try_wait(bar, parity)) return true;
   if (c.timeout_ns == 0) {
     raise_error(c, kDevTimeout);
     return false;
   }
+#pragma unroll 1
+  for (int i = 0; i < kSpinPolls; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
 #pragma unroll 1
