@@ -5,43 +5,49 @@
 // and "NVFP4 Attention QAT Backward" (cuDNN frontend docs, Overview, High-level
 // wrapper): P^ = fake_nvfp4(P) is taken of the normalised probabilities, so the
 // forward first needs LSE = ln sum_j exp(scale * Q^ K^T)_j of every query row;
-// the second pass (fwd.cu, reading this kernel's LSE) forms P, P^, O' and O.
+// the second pass (fwd_pv.cu, reading this kernel's LSE) forms P, P^, O' and O.
 //
 // This pass issues one small MMA per key tile (S on the block-scaled NVFP4
-// MMA) and is bound by the softmax warps' exp2 work and their hand-offs. A CTA
-// takes two query tiles A, B of one head and alternates between them: while
-// the softmax warps reduce S_A(j), the tensor core computes S_B(j), and the
-// other way round, so each MMA's latency hides behind the other tile's work.
-// Both tiles read the same K tile j, loaded once.
+// MMA) and is bound by the exp2 work of the softmax warps. A CTA takes two
+// query tiles A, B of one head, which share each K tile (loaded once).
+//
+// Each softmax thread owns one query row of one tile: it loads the row's 128
+// S values of a key tile from TMEM, releases the S buffer (so the next S MMA
+// of its tile can run while it computes), and keeps the row's running max and
+// sum of exp2(S * scale * log2 e) by itself. The per-tile costs of a hand-off
+// (barrier poll, TMEM load, release) are paid once per 128 keys of a row, and
+// the row's LSE needs no combining across threads. The warps of tile A and of
+// tile B share each SM sub-partition, so one tile's waits overlap the other's
+// arithmetic.
 //
 // TMEM: S_A [0,128), S_B [128,256) (one buffer each: S_X(j+1) is issued once
-// the softmax warps have read S_X(j)); scale factors of the MMAs in columns of
-// their own: Q of tile X at 256 + 8 X + 4 ks, K of key tile j at 272 + 8 (j %
-// 2) + 4 ks (4 columns per K = 64 step; lane r holds in column c the four
-// scale bytes of row r + 32 c). Key tile j + 2's K scales go into slot j % 2
-// once the last S of step j (which read it) is complete.
+// the softmax warps of tile X have loaded S_X(j)); scale factors of the MMAs in
+// columns of their own: Q of tile X at 256 + 8 X + 4 ks, K of key tile j at
+// 272 + 8 (j % 2) + 4 ks (4 columns per K = 64 step; lane r holds in column c
+// the four scale bytes of row r + 32 c). Key tile j + 2's K scales go into
+// slot j % 2 once the last S of step j (which read it) is complete; they are
+// written by the warps of tile B (of tile A when the CTA has no tile B), which
+// see every step.
 //
-// Warps (18): 0-15 softmax (warp w: lane quarter w % 4, keys 32 (w / 4) .. +31
-// of every tile; parts 1 and 3 write the K scale factors of K step part / 2);
-// 16 TMA producer; 17 MMA issuer (and TMEM allocation).
+// Warps (10): 0-7 softmax (warp w: tile w / 4, lane quarter w % 4); 8 TMA
+// producer; 9 MMA issuer (and TMEM allocation).
 #include "attn_common.cuh"
 #include "fp4_mma.cuh"
 
 namespace attnqat {
 namespace {
 
-constexpr int kSoftWarpsL = 16;
-constexpr int kWarpTmaL = 16;
-constexpr int kWarpMmaL = 17;
-constexpr int kThreadsL = 18 * 32;
+constexpr int kSoftWarpsL = 8;
+constexpr int kWarpTmaL = 8;
+constexpr int kWarpMmaL = 9;
+constexpr int kThreadsL = 10 * 32;
 
 struct LseLayout {
   static constexpr int kStages = 4;                      // NVFP4 K tiles in flight
   static constexpr uint32_t kFp4Tile = 128 * 64;         // 128 rows x 64 bytes of E2M1 pairs
   static constexpr uint32_t kQ4 = 0;                     // tile X at kQ4 + X * kFp4Tile
   static constexpr uint32_t kK0 = 2 * kFp4Tile;          // stage s at kK0 + s * kFp4Tile
-  static constexpr uint32_t kML = kK0 + kStages * kFp4Tile;   // [tile][part 1..3][row][m, l]
-  static constexpr uint32_t kBar = kML + 2 * 3 * 128 * 8;
+  static constexpr uint32_t kBar = kK0 + kStages * kFp4Tile;
   static constexpr uint32_t kBytes = kBar + 256;
   static constexpr uint32_t kAlloc = kBytes + 1024;
   static constexpr uint32_t kColSFQ = 256;               // + 8 X + 4 ks
@@ -53,9 +59,8 @@ struct LseBars {
   uint64_t q_full;
   uint64_t k_full[4], k_empty[4];
   uint64_t s_full[2];   // per tile: S_X(j) complete
-  uint64_t s_free[2];   // per tile: S_X(j) read (and, for a step's last S, key tile j + 2's K scales written)
+  uint64_t s_free[2];   // per tile: S_X(j) loaded (and, for the scale writers, key tile j + 2's K scales written)
   uint64_t sf_init;     // Q scales of both tiles, K scales of key tiles 0 and 1 written
-  uint64_t ml_ready;
   uint64_t drain;
   uint32_t tmem_base;
   uint32_t abort_flag;
@@ -73,6 +78,52 @@ struct LseArgs {
   uint64_t timeout_ns;
 };
 
+// 32 TMEM columns of this warp's 32 lanes, without waiting.
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+// Ties 32 registers to a point in the instruction stream: with `wait` set the
+// asm block also waits for this thread's TMEM loads, so no use of the
+// registers can move above the wait.
+template <bool kWait>
+__device__ __forceinline__ void tmem_tie32(uint32_t* r) {
+  if constexpr (kWait) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                   "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+  } else {
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                   "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+  }
+}
+
+__device__ __forceinline__ void tmem_st4_nowait(uint32_t taddr, const uint32_t (&r)[4]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
+               "r"(r[2]), "r"(r[3])
+               : "memory");
+}
+
 __global__ void __launch_bounds__(kThreadsL, 1)
     fwd_lse_kernel(const __grid_constant__ CUtensorMap tm_q4, const __grid_constant__ CUtensorMap tm_k4,
                    const LseArgs a) {
@@ -81,7 +132,6 @@ __global__ void __launch_bounds__(kThreadsL, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   LseBars& B = *reinterpret_cast<LseBars*>(smem + L::kBar);
-  float* ml = reinterpret_cast<float*>(smem + L::kML);
 
   const int warp = warp_id();
   const int lane = lane_id();
@@ -98,9 +148,8 @@ __global__ void __launch_bounds__(kThreadsL, 1)
     B.abort_flag = 0;
     mbar_init(&B.q_full, 1);
     for (int s = 0; s < L::kStages; ++s) mbar_init(&B.k_full[s], 1), mbar_init(&B.k_empty[s], 1);
-    for (int x = 0; x < 2; ++x) mbar_init(&B.s_full[x], 1), mbar_init(&B.s_free[x], kSoftWarpsL * 32);
-    mbar_init(&B.sf_init, 2 * 128);   // key parts 1 and 3
-    mbar_init(&B.ml_ready, 3 * 128);  // key parts 1..3
+    for (int x = 0; x < 2; ++x) mbar_init(&B.s_full[x], 1), mbar_init(&B.s_free[x], 4 * 32);   // the tile's warps
+    mbar_init(&B.sf_init, kSoftWarpsL * 32);
     mbar_init(&B.drain, 1);
     fence_mbar_init();
   }
@@ -149,11 +198,14 @@ __global__ void __launch_bounds__(kThreadsL, 1)
                      tmem + L::kColSFQ + 8 * x + 4 * ks, tmem + L::kColSFK + 8 * (j & 1) + 4 * ks, ks > 0);
         umma_commit(&B.s_full[x]);
       };
+      // Key tile j's K scales were written at step j - 2 before the scale
+      // writers released their tile's S; this thread waited for that release
+      // before issuing an S of step j - 1, so the writes precede these MMAs.
       for (int j = 0; ok && j < n_steps; ++j) {
         const int s = j % L::kStages;
         const bool kf = mbar_try_wait(&B.k_full[s], (j / L::kStages) & 1);
         const bool doA = j < nA, doB = hasB && j < nB;
-        // S_X(j) goes where S_X(j - 1) was, once the softmax warps have read it
+        // S_X(j) goes where S_X(j - 1) was, once the softmax warps have loaded it
         if (doA) {
           if ((j >= 1 && !mbar_wait(&B.s_free[0], (j - 1) & 1, ctl)) ||
               (!kf && !mbar_wait(&B.k_full[s], (j / L::kStages) & 1, ctl))) {
@@ -178,122 +230,118 @@ __global__ void __launch_bounds__(kThreadsL, 1)
       mbar_wait_drain(&B.drain, 0, ctl);
     }
   } else {
-    // ------------------------------------------------------------ softmax (warps 0-15)
-    const uint32_t quarter = warp & 3, part = warp >> 2;
-    const bool sf_writer = (part & 1u) != 0;
-    const int ks = static_cast<int>(part >> 1);
+    // ------------------------------------------------------------ softmax (warps 0-7)
+    const int x = warp >> 2;                       // tile A or B
+    const uint32_t quarter = warp & 3;
     const uint32_t r = quarter * 32 + lane;
     const uint32_t lane_off = (quarter * 32u) << 16;
+    const bool active = x == 0 || hasB;
+    const bool sf_writer = x == (hasB ? 1 : 0);   // writes the K scales (both K steps)
+    const int nX = x == 0 ? nA : nB;
+    const int qi = x == 0 ? i0 : i1;
+    const int qrow = qi * 128 + static_cast<int>(r);
+    const int kend = a.causal ? min(a.Sk, qrow + 1) : a.Sk;
     const int64_t kbase = static_cast<int64_t>(bh) * a.Sk;
-    const int qrow[2] = {i0 * 128 + static_cast<int>(r), i1 * 128 + static_cast<int>(r)};
-    const int kend[2] = {a.causal ? min(a.Sk, qrow[0] + 1) : a.Sk, a.causal ? min(a.Sk, qrow[1] + 1) : a.Sk};
-    bool ok = true;
-    // K scales written at step j (key tile j + 2's), loaded one step ahead
-    uint32_t sfw[4] = {0u, 0u, 0u, 0u};
-    if (sf_writer) {
-      uint32_t w[4];
+    auto k_scales = [&](int kt, uint32_t (&w)[2][4]) {
 #pragma unroll
-      for (int x = 0; x < 2; ++x) {
-        const int qi = x == 0 ? i0 : i1;
-        if (x == 0 || hasB) {
-          load_scales(a.q_sf, static_cast<int64_t>(bh) * a.Sq + qi * 128, min(128, a.Sq - qi * 128), ks, w);
-          tmem_st4(tmem + lane_off + L::kColSFQ + 8 * x + 4 * ks, w);
-        }
+      for (int ks = 0; ks < 2; ++ks) load_scales(a.k_sf, kbase + kt * 128, min(128, a.Sk - kt * 128), ks, w[ks]);
+    };
+    // Q scales of this warp's tile; K scales of key tiles 0, 1 (slots 0, 1)
+    // from the scale writers. Every softmax thread arrives on sf_init.
+    uint32_t sfw[2][4] = {}, sfo[2][4] = {};   // K scales written at step j (key tile j + 2's)
+    if (active) {
+      uint32_t wq[2][4], wk[2][2][4];
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks)
+        load_scales(a.q_sf, static_cast<int64_t>(bh) * a.Sq + qi * 128, min(128, a.Sq - qi * 128), ks, wq[ks]);
+      if (sf_writer) {
+#pragma unroll
+        for (int kt = 0; kt < 2; ++kt)
+          if (kt < n_steps) k_scales(kt, wk[kt]);
+        if (2 < n_steps) k_scales(2, sfw);
       }
 #pragma unroll
-      for (int kt = 0; kt < 2; ++kt) {
-        if (kt < n_steps) {
-          load_scales(a.k_sf, kbase + kt * 128, min(128, a.Sk - kt * 128), ks, w);
-          tmem_st4(tmem + lane_off + L::kColSFK + 8 * kt + 4 * ks, w);
-        }
+      for (int ks = 0; ks < 2; ++ks) tmem_st4_nowait(tmem + lane_off + L::kColSFQ + 8 * x + 4 * ks, wq[ks]);
+      if (sf_writer) {
+#pragma unroll
+        for (int kt = 0; kt < 2; ++kt)
+          if (kt < n_steps) {
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) tmem_st4_nowait(tmem + lane_off + L::kColSFK + 8 * kt + 4 * ks, wk[kt][ks]);
+          }
       }
-      if (2 < n_steps) load_scales(a.k_sf, kbase + 2 * 128, min(128, a.Sk - 2 * 128), ks, sfw);
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&B.sf_init);
     }
+    mbar_arrive(&B.sf_init);
 
     const float2 c22 = make_float2(a.c2, a.c2);
-    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.0f, 0.0f};
-    for (int j = 0; j < n_steps; ++j) {
-      const bool doA = j < nA, doB = hasB && j < nB;
-      // key tile j + 3's scales, for the write at step j + 1
-      uint32_t sfw_next[4] = {0u, 0u, 0u, 0u};
-      if (sf_writer && j + 3 < n_steps)
-        load_scales(a.k_sf, kbase + (j + 3) * 128, min(128, a.Sk - (j + 3) * 128), ks, sfw_next);
+    float m = -INFINITY, l = 0.0f;
+    // One key tile of this row: S (128 values) loaded and the buffer released,
+    // then the running max and sum updated. `sf_now` holds key tile j + 2's
+    // K scales (written here by the scale writers), `sf_next` receives key
+    // tile j + 3's (the loop alternates the two, so no copy waits for a load).
+    auto step = [&](int j, const uint32_t (&sf_now)[2][4], uint32_t (&sf_next)[2][4]) -> bool {
+      if (sf_writer && j + 3 < n_steps) k_scales(j + 3, sf_next);
+      if (!warp_wait(&B.s_full[x], j & 1, ctl)) return false;
+      tc_fence_after();
+      uint32_t v[128];
 #pragma unroll
-      for (int x = 0; x < 2; ++x) {
-        if (x == 0 ? !doA : !doB) continue;
-        if (!warp_wait(&B.s_full[x], j & 1, ctl)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_off + x * 128u + part * 32, v);
-        // the step's last S is read: both S MMAs of key tile j are complete,
-        // so key tile j + 2's K scales go into the slot they read
-        const bool last = x == 1 || !doB;
-        if (last && sf_writer && j + 2 < n_steps) tmem_st4(tmem + lane_off + L::kColSFK + 8 * (j & 1) + 4 * ks, sfw);
-        tc_fence_before();
-        mbar_arrive(&B.s_free[x]);
-        const int valid = kend[x] - (j * 128 + static_cast<int>(part) * 32);
-        if (valid < 32) {   // masked keys: -inf
+      for (int c = 0; c < 4; ++c) tmem_ld32_nowait(tmem + lane_off + x * 128u + 32 * c, v + 32 * c);
+      tmem_tie32<true>(v);
+      tmem_tie32<false>(v + 32);
+      tmem_tie32<false>(v + 64);
+      tmem_tie32<false>(v + 96);
+      // S_X(j) is loaded; for the scale writers every S of step j is complete
+      // (S_A(j) was issued before S_B(j)), so key tile j + 2's K scales go
+      // into slot j % 2, which those MMAs read
+      if (sf_writer && j + 2 < n_steps) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k)
-            if (k >= valid) v[k] = 0xFF800000u;
-        }
-        // row max of the raw S (c2 > 0: max(S) * c2 is the max of the scaled logits)
-        float mq[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          float acc = fmaxf(__uint_as_float(v[16 * u]), __uint_as_float(v[16 * u + 1]));
-#pragma unroll
-          for (int k = 2; k < 16; k += 2)
-            acc = fmax3(acc, __uint_as_float(v[16 * u + k]), __uint_as_float(v[16 * u + k + 1]));
-          mq[u] = acc;
-        }
-        const float mx = fmaxf(m[x], fmaxf(mq[0], mq[1]) * a.c2);
-        if (mx != -INFINITY) {
-          const float2 nm = make_float2(-mx, -mx);
-          float2 sc[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
-                          make_float2(0.0f, 0.0f)};
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const float2 e = ffma2(make_float2(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1])), c22, nm);
-            sc[k & 3] = fadd2(sc[k & 3], make_float2(ex2(e.x), ex2(e.y)));
-          }
-          const float2 st = fadd2(fadd2(sc[0], sc[1]), fadd2(sc[2], sc[3]));
-          l[x] = l[x] * ex2(m[x] - mx) + (st.x + st.y);
-          m[x] = mx;
-        }
+        for (int ks = 0; ks < 2; ++ks) tmem_st4_nowait(tmem + lane_off + L::kColSFK + 8 * (j & 1) + 4 * ks, sf_now[ks]);
+        tmem_wait_st();
       }
-      if (!ok) break;
+      tc_fence_before();
+      mbar_arrive(&B.s_free[x]);
+      const int valid = kend - j * 128;
+      if (valid < 128) {   // masked keys: -inf
 #pragma unroll
-      for (int q = 0; q < 4; ++q) sfw[q] = sfw_next[q];
+        for (int k = 0; k < 128; ++k)
+          if (k >= valid) v[k] = 0xFF800000u;
+      }
+      // row max of the raw S in four chains (c2 > 0: max(S) * c2 is the max
+      // of the scaled logits)
+      float mq[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        float acc = fmaxf(__uint_as_float(v[32 * u]), __uint_as_float(v[32 * u + 1]));
+#pragma unroll
+        for (int k = 2; k < 32; k += 2)
+          acc = fmax3(acc, __uint_as_float(v[32 * u + k]), __uint_as_float(v[32 * u + k + 1]));
+        mq[u] = acc;
+      }
+      const float mx = fmaxf(m, fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * a.c2);
+      if (mx == -INFINITY) return true;   // every key of the row so far masked
+      // sum of exp2(S * c2 - mx), arguments and partial sums as packed pairs
+      const float2 nm = make_float2(-mx, -mx);
+      float2 sc[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) sc[k] = make_float2(0.0f, 0.0f);
+#pragma unroll
+      for (int k = 0; k < 64; ++k) {
+        const float2 e = ffma2(make_float2(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1])), c22, nm);
+        sc[k & 7] = fadd2(sc[k & 7], make_float2(ex2(e.x), ex2(e.y)));
+      }
+      const float2 s4 = fadd2(fadd2(fadd2(sc[0], sc[1]), fadd2(sc[2], sc[3])), fadd2(fadd2(sc[4], sc[5]), fadd2(sc[6], sc[7])));
+      l = l * ex2(m - mx) + (s4.x + s4.y);
+      m = mx;
+      return true;
+    };
+    bool ok = true;
+    for (int j = 0; active && ok && j < nX; j += 2) {
+      ok = step(j, sfw, sfo);
+      if (ok && j + 1 < nX) ok = step(j + 1, sfo, sfw);
     }
-    // The four key parts of each row: parts 1..3 hand (m, l) of both tiles to
-    // part 0, which forms lse = ln sum exp(S * scale) and stores it.
-    if (ok && part != 0) {
-#pragma unroll
-      for (int x = 0; x < 2; ++x) {
-        ml[((x * 3) + (part - 1)) * 256 + r * 2] = m[x];
-        ml[((x * 3) + (part - 1)) * 256 + r * 2 + 1] = l[x];
-      }
-      mbar_arrive(&B.ml_ready);
-    } else if (ok && warp_wait(&B.ml_ready, 0, ctl)) {
-#pragma unroll
-      for (int x = 0; x < 2; ++x) {
-        if (x == 1 && !hasB) break;
-        const float* mlx = ml + x * 3 * 256;
-        float mp[4] = {m[x], mlx[r * 2], mlx[256 + r * 2], mlx[512 + r * 2]};
-        float lp[4] = {l[x], mlx[r * 2 + 1], mlx[256 + r * 2 + 1], mlx[512 + r * 2 + 1]};
-        const float M = fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3]));
-        float Lsum = 0.0f;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) Lsum += mp[q] == -INFINITY ? 0.0f : lp[q] * ex2(mp[q] - M);
-        if (qrow[x] < a.Sq) a.lse[(size_t)bh * a.Sq + qrow[x]] = (M + lg2(Lsum)) * kLn2;
-      }
-    }
+    if (active && ok && qrow < a.Sq) a.lse[(size_t)bh * a.Sq + qrow] = (m + lg2(l)) * kLn2;
   }
 
   tc_fence_before();
