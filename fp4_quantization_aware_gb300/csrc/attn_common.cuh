@@ -32,10 +32,14 @@ __device__ __forceinline__ float lg2(float x) {
   return y;
 }
 
-// Warp-uniform bounded wait: lane 0 polls, the verdict is broadcast, and the
-// warp re-converges, so warp-collective tcgen05 loads that follow are never
-// reached by only part of a warp.
+// Warp-uniform bounded wait. Every lane first polls the barrier word (one
+// shared-memory access for the warp) and a vote decides, so a phase that is
+// already complete costs no divergent branch or broadcast; otherwise lane 0
+// waits, the verdict is broadcast, and the warp re-converges. Either way the
+// warp-collective tcgen05 loads that follow are never reached by only part
+// of a warp.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const WaitCtl& c) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
   uint32_t ok = 0;
   if (lane_id() == 0) ok = mbar_wait(bar, parity, c) ? 1u : 0u;
   ok = __shfl_sync(0xffffffffu, ok, 0);
