@@ -64,8 +64,8 @@ PROFILE_INFER_JSON = os.path.join(ROOT, "profiles", "infer_kernel_ctx32k_counter
 # this GPU by a throughput probe (16 lanes x 4 sub-partitions x 2 on the
 # Blackwell Ultra SFU, whose exp throughput is twice Blackwell's).
 MUFU_EX2_PER_CLK_SM = 32
-# head groups of attnqat_bwd_host in the end-to-end measurement (c2: four
-# groups of 4 heads, one wave of CTAs each, as the whole problem takes 4 waves)
+# `chunks` of attnqat_bwd_host in the end-to-end measurement: head groups of
+# ceil(B*H / 4) heads, the first and last of half that (c2: 2, 4, 4, 4, 2)
 E2E_CHUNKS = 4
 FP4_OVER_BF16 = 6.0        # nominal dense FP4 / BF16 tensor ratio of GB300 (13.5 / 2.25 PFLOP/s)
 
@@ -637,7 +637,8 @@ def main():
         "e2e": {"value": flops_b / (r["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"], "ms": r["e2e_ms"],
                 "what": ("attnqat_bwd_host with pinned host inputs (dO, Q, K, V, O', LSE) and outputs (dQ, dK, dV); "
-                         f"{args.e2e_chunks} head groups, copies overlapping the kernels")},
+                         f"chunks={args.e2e_chunks}: head groups of ceil(B*H/{args.e2e_chunks}) heads, the first and "
+                         "last of half that, copies overlapping the kernels")},
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
     }
