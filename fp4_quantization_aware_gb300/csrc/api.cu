@@ -63,6 +63,14 @@ WsLayout layout(const attnqat_problem& p, bool bwd) {
     w.split = off,
     off += round256((split_cnt_words() + w.split_slots * split_slot_floats(to_problem(p))) * 4);
   }
+  if (!bwd && p.D == 128) {
+    // split query tiles of the forward's pass 2: counters, then the two CTAs'
+    // FP32 [O', O] slots
+    const int64_t tiles = ((p.Sq + 127) / 128) * static_cast<int64_t>(bh);
+    w.split_slots = static_cast<size_t>(tiles < kMaxSplitTiles ? tiles : kMaxSplitTiles);
+    w.split = off,
+    off += round256((split_cnt_words() + w.split_slots * fwd_split_slot_floats(to_problem(p))) * 4);
+  }
   if (p.D == 128) {   // NVFP4 Q^, K^ for the S MMAs (forward passes, backward recompute)
     w.packed = true;
     w.q4 = off, off += round256(bh * p.Sq * 64);
@@ -253,6 +261,12 @@ attnqat_status attnqat_fake_nvfp4_f32(const float* x, float* y, int64_t rows, in
   return ATTNQAT_OK;
 }
 
+// The forward's split-tile counters (D = 128), which the quantize step clears.
+int64_t fwd_split_zero_floats(const attnqat_problem& p, const WsLayout& w) {
+  (void)p;
+  return w.packed ? split_cnt_words() : 0;
+}
+
 attnqat_status attnqat_quantize_qkv(const attnqat_problem* p, const void* q, const void* k, const void* v,
                                     void* ws, size_t ws_bytes, void* stream) {
   ATTNQAT_TRY(check_problem(p));
@@ -261,7 +275,8 @@ attnqat_status attnqat_quantize_qkv(const attnqat_problem* p, const void* q, con
   ATTNQAT_TRY(check_ws(ws, ws_bytes, w.total));
   ATTNQAT_CUDA(launch_prep(to_problem(*p), static_cast<const bf16*>(q), static_cast<const bf16*>(k),
                            static_cast<const bf16*>(v), nullptr, nullptr, at<bf16>(ws, w.qh), at<bf16>(ws, w.kh),
-                           at<bf16>(ws, w.vh), nullptr, nullptr, nullptr, 0,
+                           at<bf16>(ws, w.vh), nullptr, nullptr, w.packed ? at<float>(ws, w.split) : nullptr,
+                           fwd_split_zero_floats(*p, w),
                            w.packed ? at<uint8_t>(ws, w.q4) : nullptr, w.packed ? at<uint8_t>(ws, w.qsf) : nullptr,
                            w.packed ? at<uint8_t>(ws, w.k4) : nullptr, w.packed ? at<uint8_t>(ws, w.ksf) : nullptr,
                            static_cast<cudaStream_t>(stream)),
@@ -281,7 +296,9 @@ attnqat_status attnqat_fwd_main(const attnqat_problem* p, void* o, void* o_hp, f
   ATTNQAT_CUDA(launch_fwd(to_problem(*p), at<bf16>(ws, w.qh), at<bf16>(ws, w.kh), at<bf16>(ws, w.vh),
                           w.packed ? at<uint8_t>(ws, w.q4) : nullptr, w.packed ? at<uint8_t>(ws, w.qsf) : nullptr,
                           w.packed ? at<uint8_t>(ws, w.k4) : nullptr, w.packed ? at<uint8_t>(ws, w.ksf) : nullptr,
-                          static_cast<bf16*>(o), static_cast<bf16*>(o_hp), lse, err, static_cast<cudaStream_t>(stream)),
+                          static_cast<bf16*>(o), static_cast<bf16*>(o_hp), lse,
+                          w.packed ? at<float>(ws, w.split) + split_cnt_words() : nullptr,
+                          w.packed ? at<uint32_t>(ws, w.split) : nullptr, err, static_cast<cudaStream_t>(stream)),
                "fwd_main");
   return ATTNQAT_OK;
 }
@@ -300,7 +317,8 @@ attnqat_status attnqat_fwd(const attnqat_problem* p, const void* q, const void* 
   // so the BF16 Q^, K^ are not written (V^ is: the PV MMAs read it)
   ATTNQAT_CUDA(launch_prep(to_problem(*p), static_cast<const bf16*>(q), static_cast<const bf16*>(k),
                            static_cast<const bf16*>(v), nullptr, nullptr, nullptr, nullptr, at<bf16>(ws, w.vh),
-                           nullptr, nullptr, nullptr, 0, at<uint8_t>(ws, w.q4), at<uint8_t>(ws, w.qsf),
+                           nullptr, nullptr, at<float>(ws, w.split), fwd_split_zero_floats(*p, w),
+                           at<uint8_t>(ws, w.q4), at<uint8_t>(ws, w.qsf),
                            at<uint8_t>(ws, w.k4), at<uint8_t>(ws, w.ksf), static_cast<cudaStream_t>(stream)),
                "fwd quantize");
   return attnqat_fwd_main(p, o, o_hp, lse, ws, ws_bytes, stream);

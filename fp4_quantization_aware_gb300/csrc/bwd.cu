@@ -887,7 +887,7 @@ cudaError_t launch_bwd(const Problem& p, const bf16* qh, const bf16* kh, const b
   a.scale = p.scale, a.c2 = p.scale * kLog2e;
   a.q_sf = qsf, a.k_sf = ksf;
   a.err = err, a.timeout_ns = wait_timeout_ns();
-  const BwdSplit plan = bwd_split_plan(p, device_sm_count());
+  const SplitPlan plan = bwd_split_plan(p, device_sm_count());
   a.n_full = static_cast<int>(plan.n_full);
   a.split_acc = split_acc, a.split_cnt = split_cnt;
   const int64_t blocks = plan.n_full + 2 * plan.n_split;
@@ -925,7 +925,7 @@ int device_sm_count() {
 // CTAs and r tiles left over, splitting those r tiles in two lets the last
 // wave run 2r half-length CTAs (when 2r <= SMs) instead of r full ones. A
 // problem whose every tile split fits one wave is split throughout.
-BwdSplit bwd_split_plan(const Problem& p, int sms) {
+SplitPlan bwd_split_plan(const Problem& p, int sms) {
   const int64_t nq = (p.Sq + kBlockM - 1) / kBlockM;
   const int64_t tiles = ((p.Sk + kBlockN - 1) / kBlockN) * p.bh();
   int64_t s = 0;
@@ -938,7 +938,7 @@ BwdSplit bwd_split_plan(const Problem& p, int sms) {
     }
   }
   if (s > kMaxSplitTiles) s = 0;
-  return BwdSplit{tiles - s, s};
+  return SplitPlan{tiles - s, s};
 }
 
 }  // namespace attnqat

@@ -370,7 +370,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
 
 cudaError_t launch_fwd(const Problem& p, const bf16* qh, const bf16* kh, const bf16* vh, const uint8_t* q4,
                        const uint8_t* qsf, const uint8_t* k4, const uint8_t* ksf, bf16* o, bf16* o_hp, float* lse,
-                       uint32_t* err, cudaStream_t st) {
+                       float* split_acc, uint32_t* split_cnt, uint32_t* err, cudaStream_t st) {
   if (p.D == 128) {
     // pass 1 (the LSE) in the paired kernel of fwd_lse.cu, then pass 2
     // (fwd_pv.cu) reading it; S on the block-scaled NVFP4 MMA in both
@@ -378,7 +378,7 @@ cudaError_t launch_fwd(const Problem& p, const bf16* qh, const bf16* kh, const b
       return cudaErrorInvalidValue;
     cudaError_t e = launch_fwd_lse(p, q4, qsf, k4, ksf, lse, err, st);
     if (e != cudaSuccess) return e;
-    return launch_fwd_pv(p, vh, q4, qsf, k4, ksf, lse, o, o_hp, err, st);
+    return launch_fwd_pv(p, vh, q4, qsf, k4, ksf, lse, o, o_hp, split_acc, split_cnt, err, st);
   }
   if (p.D != kD) return cudaErrorInvalidValue;
   CUtensorMap tq, tk, tv;

@@ -69,6 +69,13 @@ struct PvLayout {
   static constexpr uint32_t kColSFK = kColSFQ + 8;        // 200 (+ 8 slot + 4 ks)
   static constexpr uint32_t kColOP = 256;
   static constexpr uint32_t kColO = 384;
+  // epilogue: O' then O as BF16, each two blocks of 128 rows x 64 columns, over the V^ stages
+  static constexpr uint32_t kOutBlock = 128 * 128;
+  static_assert(4 * kOutBlock <= kStages * kVTile, "output staging fits the V^ stages");
+  // split tiles: FP32 O' then O, each four blocks of 128 rows x 32 columns,
+  // over the V^, Q and K stages (free once every MMA is done)
+  static constexpr uint32_t kSplitBlock = 128 * 32 * 4;
+  static_assert(8 * kSplitBlock <= kBar && kV0 == 0, "split staging fits below the barriers");
   static_assert(kVBlock % 1024 == 0 && kQ4 % 1024 == 0 && kK40 % 1024 == 0 && kK4Tile % 512 == 0,
                 "swizzled tiles need 1024-byte (128-byte swizzle) or 512-byte (64-byte swizzle) alignment");
   static_assert(kColSFQ % 4 == 0 && kColSFK % 4 == 0 && kColSFK + 8 * kSfSlots <= kColOP,
@@ -88,6 +95,8 @@ struct PvBars {
   uint64_t drain;
   uint32_t tmem_base;
   uint32_t abort_flag;
+  uint32_t split_order;      // split tiles: this CTA's place in the slot's count (0 or 1)
+  uint64_t split_in;         // split tiles, second CTA: the other CTA's partial rows loaded
 };
 static_assert(sizeof(PvBars) <= 512, "barrier block");
 
@@ -99,6 +108,9 @@ struct PvArgs {
   bf16* o_hp;
   int Sq, Sk;
   int n_qtiles, n_ktiles;   // 128-row query tiles, 64-key tiles
+  int n_full;               // CTAs 0 .. n_full - 1 own whole query tiles; then two CTAs per split tile
+  float* split_acc;         // split tiles: FP32 [slot][rank][O', O][128][128] (also as tm_slot)
+  uint32_t* split_cnt;      // ... and zeroed counters
   int causal;
   float c2;                 // scale * log2(e)
   uint32_t* err;
@@ -135,7 +147,9 @@ __device__ __forceinline__ void tmem_st4_nowait(uint32_t taddr, const uint32_t (
 
 __global__ void __launch_bounds__(kThreadsV, 1)
     fwd_pv_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_q4,
-                  const __grid_constant__ CUtensorMap tm_k4, const PvArgs a) {
+                  const __grid_constant__ CUtensorMap tm_k4, const __grid_constant__ CUtensorMap tm_ohp,
+                  const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_slot,
+                  const PvArgs a) {
   using L = PvLayout;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -144,10 +158,21 @@ __global__ void __launch_bounds__(kThreadsV, 1)
 
   const int warp = warp_id();
   const int lane = lane_id();
-  // Causal query tiles have 2 i + 2 key tiles: launch the longest first.
-  const int i = a.causal ? (a.n_qtiles - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
-  const int bh = blockIdx.y;
-  const int nt = a.causal ? min(a.n_ktiles, 2 * i + 2) : a.n_ktiles;
+  // 1-D grid, query tiles fastest within a head (causal: the longest first).
+  // CTA n_full + 2 u + rank works on split tile n_full + u: rank 0 takes the
+  // first half of its key tiles (rounded up), rank 1 the rest.
+  const int lin = static_cast<int>(blockIdx.x);
+  const bool split_cta = lin >= a.n_full;
+  const int sidx = split_cta ? (lin - a.n_full) >> 1 : 0;
+  const int rank = split_cta ? ((lin - a.n_full) & 1) : 0;
+  const int tile = split_cta ? a.n_full + sidx : lin;
+  const int bh = tile / a.n_qtiles;
+  const int i = a.causal ? (a.n_qtiles - 1 - tile % a.n_qtiles) : tile % a.n_qtiles;
+  const int n_total = a.causal ? min(a.n_ktiles, 2 * i + 2) : a.n_ktiles;
+  const int n_half0 = split_cta ? (n_total + 1) / 2 : n_total;
+  // this CTA's key tiles: kt0 + t for t < nt (t indexes buffers, stages and phases)
+  const int kt0 = rank == 0 ? 0 : n_half0;
+  const int nt = rank == 0 ? n_half0 : n_total - n_half0;
 
   if (threadIdx.x == 0) {
     B.abort_flag = 0;
@@ -162,6 +187,7 @@ __global__ void __launch_bounds__(kThreadsV, 1)
       mbar_init(&B.pv_read[b], 2);   // one commit each from the O' and O issuers
     }
     mbar_init(&B.o_done, 2);
+    mbar_init(&B.split_in, 1);
     mbar_init(&B.sf_init, 2 * 128);   // key parts 1 and 3
     mbar_init(&B.drain, 3);           // one commit per MMA-issuing thread
     fence_mbar_init();
@@ -180,6 +206,7 @@ __global__ void __launch_bounds__(kThreadsV, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_v), tma_prefetch_desc(&tm_q4), tma_prefetch_desc(&tm_k4);
+      tma_prefetch_desc(&tm_ohp), tma_prefetch_desc(&tm_o);
       mbar_arrive_expect_tx(&B.q_full, L::kQ4Tile);
       tma_load_3d(smem + L::kQ4, &tm_q4, &B.q_full, 0, i * 128, bh);
       int k_uses[L::kStages] = {}, v_uses[L::kStages] = {};
@@ -187,12 +214,13 @@ __global__ void __launch_bounds__(kThreadsV, 1)
         const int s = t % L::kStages, use = t / L::kStages;
         if (use >= 1 && !mbar_wait(&B.k_empty[s], (use - 1) & 1, ctl)) break;
         mbar_arrive_expect_tx(&B.k_full[s], L::kK4Tile);
-        tma_load_3d(smem + L::kK40 + s * L::kK4Tile, &tm_k4, &B.k_full[s], 0, t * kKeysV, bh);
+        tma_load_3d(smem + L::kK40 + s * L::kK4Tile, &tm_k4, &B.k_full[s], 0, (kt0 + t) * kKeysV, bh);
         ++k_uses[s];
         if (use >= 1 && !mbar_wait(&B.v_empty[s], (use - 1) & 1, ctl)) break;
         mbar_arrive_expect_tx(&B.v_full[s], L::kVTile);
         for (int h = 0; h < 2; ++h)
-          tma_load_3d(smem + L::kV0 + s * L::kVTile + h * L::kVBlock, &tm_v, &B.v_full[s], h * 64, t * kKeysV, bh);
+          tma_load_3d(smem + L::kV0 + s * L::kVTile + h * L::kVBlock, &tm_v, &B.v_full[s], h * 64, (kt0 + t) * kKeysV,
+                      bh);
         ++v_uses[s];
       }
       // every copy issued above lands before shared memory is released
@@ -278,7 +306,8 @@ __global__ void __launch_bounds__(kThreadsV, 1)
     const int qrow = i * 128 + static_cast<int>(r);
     const int kend = a.causal ? min(a.Sk, qrow + 1) : a.Sk;
     const int64_t kbase = static_cast<int64_t>(bh) * a.Sk;
-    auto k_scales = [&](int kt, uint32_t (&w)[4]) {   // rows past the tile's 64 stay 0
+    auto k_scales = [&](int t, uint32_t (&w)[4]) {   // this CTA's tile t; rows past the tile's 64 stay 0
+      const int kt = kt0 + t;
       load_scales(a.k_sf, kbase + static_cast<int64_t>(kt) * kKeysV, min(kKeysV, a.Sk - kt * kKeysV), ks, w);
     };
     // K scales written at tile t (those of tile t + 3), loaded one tile ahead.
@@ -307,7 +336,7 @@ __global__ void __launch_bounds__(kThreadsV, 1)
     // loop below alternates the two arrays, so no copy waits for the load).
     auto tile = [&](int t, const uint32_t (&sf_now)[4], uint32_t (&sf_next)[4]) -> bool {
       const int b = t % kRing;
-      const int valid = kend - (t * kKeysV + static_cast<int>(part) * kPartKeys);
+      const int valid = kend - ((kt0 + t) * kKeysV + static_cast<int>(part) * kPartKeys);
       if (sf_writer && t + kRing + 1 < nt) k_scales(t + kRing + 1, sf_next);
       if (!warp_wait(&B.s_full[b], (t / kRing) & 1, ctl)) return false;
       tc_fence_after();
@@ -355,18 +384,127 @@ __global__ void __launch_bounds__(kThreadsV, 1)
       if (ok && t + 1 < nt) ok = tile(t + 1, sfo, sfw);
     }
     // epilogue: part p stores columns [128 / kParts p, + 128 / kParts) of O'
-    // and O (a one-shot barrier committed after the last O' and O MMAs)
-    if (ok && warp_wait(&B.o_done, 0, ctl)) {
-      tc_fence_after();
-      const size_t row = static_cast<size_t>(bh) * a.Sq + qrow;
-      uint32_t v[32];
+    // and O (a one-shot barrier committed after the last O' and O MMAs). The
+    // two CTAs of a split tile store their FP32 rows in the tile's slot; the
+    // one that counts second adds the other's and stores the BF16 sums.
+    const bool have = ok && nt > 0 && warp_wait(&B.o_done, 0, ctl);
+    if (have) tc_fence_after();
+    constexpr int kCols = 128 / kParts;
+    if (!split_cta) {
+      // O' and O as BF16 in the free V^ area (all O', O MMAs are done), two
+      // 64-column 128-byte-swizzled blocks each, then four TMA stores, so the
+      // rows go out coalesced (rows past Sq are clipped by the tensor maps)
+      if (have) {
 #pragma unroll
-      for (int c = 0; c < 128 / kParts; c += 32) {
-        const uint32_t col = part * (128 / kParts) + c;
-        tmem_ld32(tmem + lane_off + L::kColOP + col, v);
-        if (qrow < a.Sq) store_row32_bf16(a.o_hp + row * 128 + col, v, 1.0f);
-        tmem_ld32(tmem + lane_off + L::kColO + col, v);
-        if (qrow < a.Sq) store_row32_bf16(a.o + row * 128 + col, v, 1.0f);
+        for (int o = 0; o < 2; ++o) {
+#pragma unroll
+          for (int c = 0; c < kCols; c += 32) {
+            const uint32_t col = part * kCols + c;
+            uint32_t v[32], w[16];
+            tmem_ld32(tmem + lane_off + (o == 0 ? L::kColOP : L::kColO) + col, v);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) w[k] = pack_bf16x2(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]));
+            const uint32_t blk = sbase + L::kV0 + o * 2 * L::kOutBlock + (col / 64) * L::kOutBlock;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              st_shared_v4(sw128_chunk(blk, r, (col % 64) / 8 + j), w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+          }
+        }
+        fence_proxy_async_smem();
+      }
+      named_bar_sync(1, kSoftWarpsV * 32);
+      if (have && warp == 0 && lane == 0) {
+#pragma unroll
+        for (int o = 0; o < 2; ++o)
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            tma_store_3d(o == 0 ? &tm_ohp : &tm_o, smem + L::kV0 + (2 * o + h) * L::kOutBlock, 64 * h, i * 128, bh);
+        bulk_commit_group();
+        bulk_wait_group<0>();
+      }
+    } else {
+      // The two CTAs of a split tile: each stages its FP32 partial O' and O
+      // rows in shared memory (the free V^, Q, K stages: eight 128-row x
+      // 32-column blocks, 128-byte swizzled) and stores them to its slot with
+      // TMA; the one that counts second loads the other's slot back with TMA,
+      // adds its own partial and stores the BF16 sums as the whole tiles do.
+      uint32_t v[2][32];
+#pragma unroll
+      for (int o = 0; o < 2; ++o) {
+        if (have) {
+          tmem_ld32(tmem + lane_off + (o == 0 ? L::kColOP : L::kColO) + part * 32, v[o]);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[o][k] = 0u;   // no key tiles: adds nothing
+        }
+        const uint32_t blk = sbase + (o * 4 + part) * L::kSplitBlock;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          st_shared_v4(sw128_chunk(blk, r, j), v[o][4 * j], v[o][4 * j + 1], v[o][4 * j + 2], v[o][4 * j + 3]);
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, kSoftWarpsV * 32);
+      const int row0 = (sidx * 2 + rank) * 2 * 128, orow0 = (sidx * 2 + (rank ^ 1)) * 2 * 128;
+      if (warp == 0 && lane == 0) {
+#pragma unroll
+        for (int o = 0; o < 2; ++o)
+#pragma unroll
+          for (int pp = 0; pp < 4; ++pp)
+            tma_store_3d(&tm_slot, smem + (o * 4 + pp) * L::kSplitBlock, 32 * pp, row0 + o * 128, 0);
+        bulk_commit_group();
+        bulk_wait_group<0>();        // this CTA's rows are written (and its staging read)
+        fence_proxy_async_all();
+        __threadfence();
+        B.split_order = atomicAdd(a.split_cnt + sidx, 1u);
+        if (B.split_order == 1u) {   // the other CTA's rows are written too
+          __threadfence();
+          fence_proxy_async_all();
+          mbar_arrive_expect_tx(&B.split_in, 8 * L::kSplitBlock);
+#pragma unroll
+          for (int o = 0; o < 2; ++o)
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp)
+              tma_load_3d(smem + (o * 4 + pp) * L::kSplitBlock, &tm_slot, &B.split_in, 32 * pp, orow0 + o * 128, 0);
+        }
+      }
+      named_bar_sync(1, kSoftWarpsV * 32);
+      if (*reinterpret_cast<volatile uint32_t*>(&B.split_order) == 1u) {
+        const bool in = warp_wait(&B.split_in, 0, ctl);
+#pragma unroll
+        for (int o = 0; o < 2; ++o) {
+          const uint32_t blk = (o * 4 + part) * L::kSplitBlock;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 x = *reinterpret_cast<const float4*>(smem + (sw128_chunk(sbase + blk, r, j) - sbase));
+            v[o][4 * j] = __float_as_uint(__uint_as_float(v[o][4 * j]) + x.x);
+            v[o][4 * j + 1] = __float_as_uint(__uint_as_float(v[o][4 * j + 1]) + x.y);
+            v[o][4 * j + 2] = __float_as_uint(__uint_as_float(v[o][4 * j + 2]) + x.z);
+            v[o][4 * j + 3] = __float_as_uint(__uint_as_float(v[o][4 * j + 3]) + x.w);
+          }
+        }
+        named_bar_sync(1, kSoftWarpsV * 32);   // every thread has read the FP32 blocks
+#pragma unroll
+        for (int o = 0; o < 2; ++o) {
+          uint32_t w[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) w[k] = pack_bf16x2(__uint_as_float(v[o][2 * k]), __uint_as_float(v[o][2 * k + 1]));
+          const uint32_t col = part * 32;
+          const uint32_t blk = sbase + L::kV0 + o * 2 * L::kOutBlock + (col / 64) * L::kOutBlock;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            st_shared_v4(sw128_chunk(blk, r, (col % 64) / 8 + j), w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, kSoftWarpsV * 32);
+        if (in && warp == 0 && lane == 0) {
+#pragma unroll
+          for (int o = 0; o < 2; ++o)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              tma_store_3d(o == 0 ? &tm_ohp : &tm_o, smem + L::kV0 + (2 * o + h) * L::kOutBlock, 64 * h, i * 128, bh);
+          bulk_commit_group();
+          bulk_wait_group<0>();
+        }
       }
     }
   }
@@ -383,14 +521,16 @@ __global__ void __launch_bounds__(kThreadsV, 1)
 
 cudaError_t launch_fwd_pv(const Problem& p, const bf16* vh, const uint8_t* q4, const uint8_t* qsf,
                           const uint8_t* k4, const uint8_t* ksf, const float* lse, bf16* o, bf16* o_hp,
-                          uint32_t* err, cudaStream_t st) {
+                          float* split_acc, uint32_t* split_cnt, uint32_t* err, cudaStream_t st) {
   if (p.D != 128 || vh == nullptr || q4 == nullptr || qsf == nullptr || k4 == nullptr || ksf == nullptr ||
       lse == nullptr)
     return cudaErrorInvalidValue;
   CUtensorMap tv, tq4, tk4;
   const uint64_t bh = p.bh();
+  CUtensorMap tohp, to;
   if (!make_tile_map(&tv, vh, false, 128, p.Sk, bh, 64, kKeysV) || !make_fp4_map(&tq4, q4, p.Sq, bh, 128) ||
-      !make_fp4_map(&tk4, k4, p.Sk, bh, kKeysV))
+      !make_fp4_map(&tk4, k4, p.Sk, bh, kKeysV) || !make_tile_map(&tohp, o_hp, false, 128, p.Sq, bh, 64, 128) ||
+      !make_tile_map(&to, o, false, 128, p.Sq, bh, 64, 128))
     return cudaErrorInvalidValue;
   PvArgs a;
   a.q_sf = qsf, a.k_sf = ksf, a.lse = lse;
@@ -401,11 +541,42 @@ cudaError_t launch_fwd_pv(const Problem& p, const bf16* vh, const uint8_t* q4, c
   a.causal = p.causal ? 1 : 0;
   a.c2 = p.scale * kLog2e;
   a.err = err, a.timeout_ns = wait_timeout_ns();
+  const SplitPlan plan = fwd_pv_split_plan(p, device_sm_count());
+  a.n_full = static_cast<int>(plan.n_full);
+  a.split_acc = split_acc, a.split_cnt = split_cnt;
+  const int64_t blocks = plan.n_full + 2 * plan.n_split;
+  if (blocks > 0x7fffffff || (plan.n_split > 0 && (split_acc == nullptr || split_cnt == nullptr)))
+    return cudaErrorInvalidValue;
+  // the split slots as one FP32 matrix of [slot][rank][O', O] 128-row blocks,
+  // 128 columns, read and written in 32-column boxes
+  CUtensorMap tslot = tv;   // not read without split tiles
+  if (plan.n_split > 0 && !make_tile_map(&tslot, split_acc, true, 128, static_cast<uint64_t>(plan.n_split) * 4 * 128, 1,
+                                         32, 128))
+    return cudaErrorInvalidValue;
   cudaError_t e = set_smem(reinterpret_cast<const void*>(&fwd_pv_kernel), PvLayout::kAlloc);
   if (e != cudaSuccess) return e;
-  const dim3 grid(static_cast<unsigned>(a.n_qtiles), static_cast<unsigned>(bh));
-  fwd_pv_kernel<<<grid, kThreadsV, PvLayout::kAlloc, st>>>(tv, tq4, tk4, a);
+  fwd_pv_kernel<<<static_cast<unsigned>(blocks), kThreadsV, PvLayout::kAlloc, st>>>(tv, tq4, tk4, tohp, to, tslot, a);
   return cudaGetLastError();
+}
+
+// The query tiles of a partial last wave (or, when every tile's two halves fit
+// one wave, all of them) get two CTAs each, as in the backward: the key loop
+// of a non-causal tile splits evenly, and two halves of a tile take about 0.6
+// of a whole tile's time.
+SplitPlan fwd_pv_split_plan(const Problem& p, int sms) {
+  const int64_t nk = (p.Sk + kKeysV - 1) / kKeysV;
+  const int64_t tiles = ((p.Sq + 127) / 128) * p.bh();
+  int64_t s = 0;
+  if (nk >= 2 && sms > 0) {
+    if (2 * tiles <= sms) {
+      s = tiles;
+    } else if (!p.causal) {
+      const int64_t r = tiles % sms;
+      s = 2 * r <= sms ? r : 0;
+    }
+  }
+  if (s > kMaxSplitTiles) s = 0;
+  return SplitPlan{tiles - s, s};
 }
 
 }  // namespace attnqat

@@ -47,7 +47,7 @@ cudaError_t launch_dq_convert(const Problem& p, const float* dq_acc, bf16* dq, c
 // block-scaled S (D = 128; null for D = 64, which stays on BF16).
 cudaError_t launch_fwd(const Problem& p, const bf16* qh, const bf16* kh, const bf16* vh, const uint8_t* q4,
                        const uint8_t* qsf, const uint8_t* k4, const uint8_t* ksf, bf16* o, bf16* o_hp, float* lse,
-                       uint32_t* err, cudaStream_t st);
+                       float* split_acc, uint32_t* split_cnt, uint32_t* err, cudaStream_t st);
 
 // Pass 1 of the D = 128 forward: the natural-log LSE of every query row, two
 // query tiles of a head per CTA (S on the block-scaled NVFP4 MMA).
@@ -57,24 +57,32 @@ cudaError_t launch_fwd_lse(const Problem& p, const uint8_t* q4, const uint8_t* q
 // Pass 2 of the D = 128 forward: O' = P V^ and O = fake_nvfp4(P) V^ from pass
 // 1's LSE, one 128-row query tile per CTA over 64-key tiles (S on the
 // block-scaled NVFP4 MMA).
+// The query tiles of fwd_pv_split_plan's split share two CTAs each, which
+// store their FP32 partial O', O rows in slots of split_acc (fwd_split_slot_floats
+// each); the one that counts second (counters at split_cnt, zeroed) adds them.
 cudaError_t launch_fwd_pv(const Problem& p, const bf16* vh, const uint8_t* q4, const uint8_t* qsf,
                           const uint8_t* k4, const uint8_t* ksf, const float* lse, bf16* o, bf16* o_hp,
-                          uint32_t* err, cudaStream_t st);
+                          float* split_acc, uint32_t* split_cnt, uint32_t* err, cudaStream_t st);
 
-// How the backward shares key tiles between CTAs: the first n_full key tiles
+// How a kernel shares its work units between CTAs: the first n_full units
 // (in grid order) get one CTA each, the last n_split two CTAs each (half the
-// query tiles apiece), whose FP32 partial dK, dV meet in a workspace slot.
+// unit's loop apiece), whose FP32 partial results meet in a workspace slot.
+// The backward's units are key tiles (its loop runs over query tiles), the
+// forward pass 2's are query tiles (its loop runs over key tiles).
 constexpr int64_t kMaxSplitTiles = 96;
-struct BwdSplit {
+struct SplitPlan {
   int64_t n_full, n_split;
 };
-BwdSplit bwd_split_plan(const Problem& p, int sms);
+SplitPlan bwd_split_plan(const Problem& p, int sms);
+SplitPlan fwd_pv_split_plan(const Problem& p, int sms);
 int device_sm_count();   // SMs of the current device (148 if it cannot be read)
 
 // Split-tile workspace: kMaxSplitTiles counters (rounded to 64 words), then
-// min(tiles, kMaxSplitTiles) slots of [dK, dV][128][D] FP32.
+// min(tiles, kMaxSplitTiles) slots of two FP32 [128][D] outputs ([dK, dV] in
+// the backward, [O', O] in the forward).
 inline int64_t split_cnt_words() { return 64 * ((kMaxSplitTiles + 63) / 64); }
 inline int64_t split_slot_floats(const Problem& p) { return 2 * 128 * p.D; }
+inline int64_t fwd_split_slot_floats(const Problem& p) { return 2 * 2 * 128 * p.D; }   // both ranks' [O', O]
 
 // The forward in recipe R2 (one pass; P^ of each key tile quantized before
 // normalisation) from the quantize step's Q^, K^, V^; same outputs as launch_fwd.

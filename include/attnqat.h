@@ -143,7 +143,10 @@ attnqat_status attnqat_bwd_host(const attnqat_problem* p, const void* dout, cons
 /* ---- the steps of attnqat_fwd / attnqat_bwd, for callers that time or
  * schedule them separately. Each takes the same workspace. ---- */
 
-/* Forward step 1: Q^, K^, V^ into the workspace (HBM-bound). */
+/* Forward step 1: Q^, K^, V^ into the workspace (HBM-bound). At D = 128 it
+ * also clears the counters with which step 2 combines the partial outputs of
+ * its split query tiles, so each attnqat_fwd_main needs an
+ * attnqat_quantize_qkv on the same workspace before it. */
 attnqat_status attnqat_quantize_qkv(const attnqat_problem* p, const void* q, const void* k, const void* v,
                                     void* workspace, size_t workspace_bytes, void* stream);
 

@@ -68,8 +68,11 @@ def test_workspace_sizes(clib):
     bh = 16
     fwd = clib.attnqat_fwd_workspace_bytes(ctypes.byref(p))
     bwd = clib.attnqat_bwd_workspace_bytes(ctypes.byref(p))
-    # Q^, K^, V^ (BF16) and, at D = 128, NVFP4 Q and K (E2M1 pairs + E4M3 scales)
-    assert fwd == 3 * bh * 4096 * 128 * 2 + 2 * (bh * 4096 * 64 + bh * 4096 * 8)
+    # Q^, K^, V^ (BF16) and, at D = 128, the split-tile area of pass 2 (128
+    # counter words and, for min(query tiles, 96) tiles, both CTAs' FP32 [O', O]
+    # slots) and NVFP4 Q and K (E2M1 pairs + E4M3 scales)
+    fsplit = 128 * 4 + min(bh * 4096 // 128, 96) * 2 * 2 * 128 * 128 * 4
+    assert fwd == 3 * bh * 4096 * 128 * 2 + fsplit + 2 * (bh * 4096 * 64 + bh * 4096 * 8)
     base = 3 * bh * 4096 * 128 * 2
     # + delta, the FP32 dQ accumulator, the split-tile area (128 counter words
     # and FP32 [dK, dV] slots for min(key tiles, 96) tiles) and, at D = 128,
