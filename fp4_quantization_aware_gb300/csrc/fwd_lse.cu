@@ -162,6 +162,10 @@ __global__ void __launch_bounds__(kThreadsL, 1)
   tc_fence_after();
   const uint32_t tmem = B.tmem_base;
   const WaitCtl ctl{&B.abort_flag, a.err, a.timeout_ns};
+  // launched as a programmatic dependent of the quantize step: its NVFP4 Q,
+  // K and scales are read after grid_dep_wait; pass 2 may then start
+  grid_dep_wait();
+  grid_dep_launch();
 
   if (warp == kWarpTmaL) {
     // ------------------------------------------------------------ producer
@@ -372,8 +376,7 @@ cudaError_t launch_fwd_lse(const Problem& p, const uint8_t* q4, const uint8_t* q
   const dim3 grid(static_cast<unsigned>(a.n_pairs), static_cast<unsigned>(bh));
   cudaError_t e = set_smem(reinterpret_cast<const void*>(&fwd_lse_kernel), LseLayout::kAlloc);
   if (e != cudaSuccess) return e;
-  fwd_lse_kernel<<<grid, kThreadsL, LseLayout::kAlloc, st>>>(tq4, tk4, a);
-  return cudaGetLastError();
+  return launch_dependent(fwd_lse_kernel, grid, dim3(kThreadsL), LseLayout::kAlloc, st, tq4, tk4, a);
 }
 
 }  // namespace attnqat

@@ -201,6 +201,9 @@ __global__ void __launch_bounds__(kThreadsV, 1)
   tc_fence_after();
   const uint32_t tmem = B.tmem_base;
   const WaitCtl ctl{&B.abort_flag, a.err, a.timeout_ns};
+  // Launched as a programmatic dependent of the LSE pass, which let this one
+  // start only after the quantize step had completed: its NVFP4 Q, K, scales
+  // and V^ are readable now, the LSE only after grid_dep_wait (softmax warps).
 
   if (warp == kWarpTmaV) {
     // ------------------------------------------------------------ producer
@@ -328,6 +331,7 @@ __global__ void __launch_bounds__(kThreadsV, 1)
       tc_fence_before();
       mbar_arrive(&B.sf_init);
     }
+    grid_dep_wait();
     const float lse2 = qrow < a.Sq ? __ldg(a.lse + static_cast<size_t>(bh) * a.Sq + qrow) * kLog2e : 0.0f;
     const float2 c22 = make_float2(a.c2, a.c2), nl = make_float2(-lse2, -lse2);
     // One tile: P = exp2(S c2 - lse2), P^ = fake_nvfp4(P) over this warp's S
@@ -555,8 +559,8 @@ cudaError_t launch_fwd_pv(const Problem& p, const bf16* vh, const uint8_t* q4, c
     return cudaErrorInvalidValue;
   cudaError_t e = set_smem(reinterpret_cast<const void*>(&fwd_pv_kernel), PvLayout::kAlloc);
   if (e != cudaSuccess) return e;
-  fwd_pv_kernel<<<static_cast<unsigned>(blocks), kThreadsV, PvLayout::kAlloc, st>>>(tv, tq4, tk4, tohp, to, tslot, a);
-  return cudaGetLastError();
+  return launch_dependent(fwd_pv_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kThreadsV), PvLayout::kAlloc, st,
+                          tv, tq4, tk4, tohp, to, tslot, a);
 }
 
 // The query tiles of a partial last wave (or, when every tile's two halves fit

@@ -8,6 +8,21 @@ namespace attnqat {
 
 using bf16 = __nv_bfloat16;
 
+// Launch `kernel` as a programmatic dependent of the previous kernel in the
+// stream: its CTAs may start while that kernel finishes, and the kernel waits
+// (grid_dep_wait) before it reads that kernel's results.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid, cfg.blockDim = block, cfg.dynamicSmemBytes = smem, cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr, cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 struct Problem {
   int64_t B, H, Sq, Sk, D;
   bool causal;

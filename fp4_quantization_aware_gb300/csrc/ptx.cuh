@@ -145,6 +145,17 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // every state space, global included.
 __device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// A kernel launched as a programmatic dependent of the previous kernel in the
+// stream may start before that kernel ends. grid_dep_wait returns once the
+// previous kernel has completed and its writes are visible (at once for a
+// kernel launched without the dependency); a kernel calls it before reading
+// what that kernel wrote. grid_dep_launch lets the next kernel start early;
+// the forward's LSE pass calls it only after its own grid_dep_wait, so pass 2
+// (its dependent) may read the quantize step's outputs at once.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
