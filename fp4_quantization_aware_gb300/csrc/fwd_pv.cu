@@ -424,7 +424,7 @@ __global__ void __launch_bounds__(kThreadsV, 1)
           for (int h = 0; h < 2; ++h)
             tma_store_3d(o == 0 ? &tm_ohp : &tm_o, smem + L::kV0 + (2 * o + h) * L::kOutBlock, 64 * h, i * 128, bh);
         bulk_commit_group();
-        bulk_wait_group<0>();
+        bulk_wait_group_read<0>();   // shared memory read: the CTA may exit
       }
     } else {
       // The two CTAs of a split tile: each stages its FP32 partial O' and O
@@ -507,7 +507,7 @@ __global__ void __launch_bounds__(kThreadsV, 1)
             for (int h = 0; h < 2; ++h)
               tma_store_3d(o == 0 ? &tm_ohp : &tm_o, smem + L::kV0 + (2 * o + h) * L::kOutBlock, 64 * h, i * 128, bh);
           bulk_commit_group();
-          bulk_wait_group<0>();
+          bulk_wait_group_read<0>();
         }
       }
     }

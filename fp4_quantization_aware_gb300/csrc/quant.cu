@@ -8,7 +8,9 @@
 //  - the bounded-wait self-test.
 // One thread owns one 16-value group (32 bytes of BF16): a warp moves 1 KiB
 // contiguous per access, and the D/16 threads of a row reduce delta with
-// shuffles.
+// shuffles. (Two or four groups per thread with every load issued first was
+// slower here: twice the registers halve the CTAs resident per SM.) The dQ
+// conversion gives a thread four float4s a block apart, loaded first.
 #include "kernels.h"
 #include "nvfp4.cuh"
 
@@ -16,6 +18,7 @@ namespace attnqat {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kConvU = 4;   // float4 per dQ-conversion thread
 
 __device__ __forceinline__ void unpack8(const uint4& u, float* f) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -168,12 +171,18 @@ __global__ void __launch_bounds__(kThreads) prep_kernel(PrepArgs a) {
   if (live && (g % kGroupsPerRow) == 0) a.delta[g / kGroupsPerRow] = part;
 }
 
+// Thread x of block b converts float4s (b kConvU + u) kThreads + x.
 __global__ void __launch_bounds__(kThreads) dq_convert_kernel(const float4* __restrict__ acc, uint2* __restrict__ dq,
                                                               int64_t n4) {
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
-  if (i >= n4) return;
-  const float4 v = acc[i];
-  dq[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * (kThreads * kConvU) + threadIdx.x;
+  float4 v[kConvU];
+#pragma unroll
+  for (int u = 0; u < kConvU; ++u)
+    if (i0 + u * kThreads < n4) v[u] = acc[i0 + u * kThreads];
+#pragma unroll
+  for (int u = 0; u < kConvU; ++u)
+    if (i0 + u * kThreads < n4)
+      dq[i0 + u * kThreads] = make_uint2(pack_bf16x2(v[u].x, v[u].y), pack_bf16x2(v[u].z, v[u].w));
 }
 
 // One CTA waits on a barrier that nothing arrives at; the bounded wait gives
@@ -338,8 +347,9 @@ cudaError_t launch_nvfp4_pack(const bf16* x, uint8_t* packed, uint8_t* scales, i
 
 cudaError_t launch_dq_convert(const Problem& p, const float* dq_acc, bf16* dq, cudaStream_t st) {
   const int64_t n4 = p.bh() * p.Sq * p.D / 4;
-  dq_convert_kernel<<<blocks_for(n4), kThreads, 0, st>>>(reinterpret_cast<const float4*>(dq_acc),
-                                                         reinterpret_cast<uint2*>(dq), n4);
+  if (n4 == 0) return cudaSuccess;
+  dq_convert_kernel<<<blocks_for((n4 + kConvU - 1) / kConvU), kThreads, 0, st>>>(
+      reinterpret_cast<const float4*>(dq_acc), reinterpret_cast<uint2*>(dq), n4);
   return cudaGetLastError();
 }
 
