@@ -17,6 +17,9 @@ from typing import Optional
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libattnqat.so")
+# the debug build: bounds checks on every plain global access, counted
+# (attnqat_debug_oob_count); for tests, loaded with load(CHECKED_LIB_PATH)
+CHECKED_LIB_PATH = os.path.join(HERE, "libattnqat_checked.so")
 
 ATTNQAT_OK = 0
 # probability quantizers of recipe R2 (attnqat_p_format)
@@ -71,6 +74,9 @@ SIGNATURES = {
     "attnqat_fwd_main_r2": (_S, [_PP, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "attnqat_fwd_r2_p": (_S, [_PP, _P, _P, _P, _P, _P, _P, ctypes.c_int, _P, ctypes.c_size_t, _P]),
     "attnqat_fwd_main_r2_p": (_S, [_PP, _P, _P, _P, ctypes.c_int, _P, ctypes.c_size_t, _P]),
+    "attnqat_checked_build": (ctypes.c_int, []),
+    "attnqat_debug_oob_count": (_S, [ctypes.POINTER(ctypes.c_ulonglong), ctypes.c_int]),
+    "attnqat_selftest_bounds": (_S, [_P, ctypes.c_int64, ctypes.c_int64, _P]),
 }
 
 _lib = None

@@ -1,6 +1,8 @@
-"""Build libattnqat.so in-tree for sm_103a with nvcc (no cmake, one -gencode).
+"""Build libattnqat.so in-tree for sm_103a with nvcc (no cmake, one -gencode),
+and the debug build libattnqat_checked.so (the same sources with
+-DATTNQAT_CHECKED: bounds checks on every plain global access, counted).
 
-Usage: python -m fp4_quantization_aware_gb300.build [--verbose]
+Usage: python -m fp4_quantization_aware_gb300.build [--verbose] [--checked]
 The translation units compile in parallel; the library links the CUDA
 runtime statically, so loading it needs no libcudart on the library path.
 """
@@ -16,6 +18,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libattnqat.so")
+BUILD_CHECKED = os.path.join(HERE, "_build_checked")
+LIB_CHECKED = os.path.join(HERE, "libattnqat_checked.so")
 SOURCES = ["api.cu", "quant.cu", "fwd.cu", "fwd_lse.cu", "fwd_pv.cu", "fwd_r2.cu", "bwd.cu", "infer.cu", "noalloc.cu", "host.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
@@ -29,9 +33,9 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def _compile(src: str, verbose: bool) -> str:
-    obj = os.path.join(BUILD, src.replace(".cu", ".o"))
-    cmd = [nvcc(), *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+def _compile(src: str, verbose: bool, checked: bool = False) -> str:
+    obj = os.path.join(BUILD_CHECKED if checked else BUILD, src.replace(".cu", ".o"))
+    cmd = [nvcc(), *ARCH, *FLAGS, *(["-DATTNQAT_CHECKED"] if checked else []), "-c", os.path.join(CSRC, src), "-o", obj]
     if verbose:
         cmd += ["-Xptxas", "-v"]
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -42,21 +46,23 @@ def _compile(src: str, verbose: bool) -> str:
     return obj
 
 
-def build(verbose: bool = False, force: bool = False) -> str:
-    """Compile every CUDA source and link libattnqat.so; returns its path."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, force: bool = False, checked: bool = False) -> str:
+    """Compile every CUDA source and link libattnqat.so (checked: the debug
+    build libattnqat_checked.so); returns its path."""
+    lib = LIB_CHECKED if checked else LIB
+    os.makedirs(BUILD_CHECKED if checked else BUILD, exist_ok=True)
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(HERE, "..", "include", "attnqat.h")]
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= max(os.path.getmtime(d) for d in deps):
-        return LIB
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= max(os.path.getmtime(d) for d in deps):
+        return lib
     with concurrent.futures.ThreadPoolExecutor(len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose), SOURCES))
-    tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, verbose, checked), SOURCES))
+    tmp = lib + ".tmp"
     r = subprocess.run([nvcc(), *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(verbose="--verbose" in sys.argv, force=True))
+    print(build(verbose="--verbose" in sys.argv, force=True, checked="--checked" in sys.argv))

@@ -508,6 +508,33 @@ attnqat_status attnqat_device_status(int clear) {
   return v == kDevTimeout ? fail(ATTNQAT_ERR_TIMEOUT, "a device wait ran out of time") : ATTNQAT_OK;
 }
 
+int attnqat_checked_build(void) {
+#ifdef ATTNQAT_CHECKED
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+attnqat_status attnqat_debug_oob_count(unsigned long long* count, int clear) {
+  ATTNQAT_TRY(check_ptrs({count}));
+  if (!attnqat_checked_build()) return fail(ATTNQAT_ERR_UNSUPPORTED, "bounds checks are in the debug build only");
+  ATTNQAT_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
+  unsigned long long n = 0;
+  for (auto* rd : {oob_read_fwd_lse, oob_read_fwd_pv, oob_read_fwd, oob_read_fwd_r2, oob_read_bwd, oob_read_infer,
+                   oob_read_quant})
+    ATTNQAT_CUDA(rd(&n, clear != 0), "read bounds-check counters");
+  *count = n;
+  return ATTNQAT_OK;
+}
+
+attnqat_status attnqat_selftest_bounds(float* buf, int64_t n, int64_t extra, void* stream) {
+  if (!attnqat_checked_build()) return fail(ATTNQAT_ERR_UNSUPPORTED, "bounds checks are in the debug build only");
+  if (buf == nullptr || n < 1 || extra < 0) return fail(ATTNQAT_ERR_INVALID_ARG, "buf null, n < 1 or extra < 0");
+  ATTNQAT_CUDA(launch_bounds_selftest(buf, n, extra, static_cast<cudaStream_t>(stream)), "selftest_bounds");
+  return ATTNQAT_OK;
+}
+
 attnqat_status attnqat_selftest_quotient(unsigned long long* out, void* stream) {
   ATTNQAT_TRY(check_ptrs({out}));
   ATTNQAT_CUDA(launch_quotient_selftest(out, static_cast<cudaStream_t>(stream)), "selftest_quotient");

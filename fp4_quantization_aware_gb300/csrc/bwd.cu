@@ -42,6 +42,7 @@
 // dQ staging 32K.
 #include "attn_common.cuh"
 #include "fp4_mma.cuh"
+#include "checked.cuh"
 
 namespace attnqat {
 namespace {
@@ -110,6 +111,7 @@ struct BwdArgs {
   const uint8_t* k_sf;
   uint32_t* err;
   uint64_t timeout_ns;
+  ATTNQAT_CHECKED_ONLY(int64_t rows_q; int64_t rows_k; int64_t n_split;)   // debug build: B*H*Sq, B*H*Sk, split tiles
 };
 
 // Epilogue of the softmax warps (256 threads): warps 0-3 own dK rows, warps
@@ -130,13 +132,14 @@ __device__ __forceinline__ void store_dk_dv(const BwdArgs& a, uint32_t tcol, boo
       for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(tcol + c * 32, v);
-        if (krow < a.Sk) store_row32_bf16(out + c * 32, v, 1.0f);
+        if (krow < a.Sk && ATTNQAT_IN_BOUNDS(static_cast<int64_t>(bh) * a.Sk + krow < a.rows_k))
+          store_row32_bf16(out + c * 32, v, 1.0f);
       }
     }
     return;
   }
   float* slot = a.split_acc + ((size_t)(sidx * 2 + half) * 128 + r) * D;
-  if (have) {
+  if (have && ATTNQAT_IN_BOUNDS(sidx < a.n_split)) {
 #pragma unroll 1
     for (int c = 0; c < D / 32; ++c) {
       uint32_t v[32];
@@ -149,11 +152,11 @@ __device__ __forceinline__ void store_dk_dv(const BwdArgs& a, uint32_t tcol, boo
   }
   __threadfence();
   named_bar_sync(1, 256);                                  // all partial rows of this CTA are added
-  if (leader) *split_order = atomicAdd(a.split_cnt + sidx, 1u);
+  if (leader) *split_order = ATTNQAT_IN_BOUNDS(sidx < a.n_split) ? atomicAdd(a.split_cnt + sidx, 1u) : 0u;
   named_bar_sync(1, 256);
   if (*reinterpret_cast<volatile uint32_t*>(split_order) == 1u) {   // the other CTA's rows are in too
     __threadfence();
-    if (krow < a.Sk) {
+    if (krow < a.Sk && ATTNQAT_IN_BOUNDS(static_cast<int64_t>(bh) * a.Sk + krow < a.rows_k)) {
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
@@ -350,7 +353,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
     auto row_stats = [&](int it, float& lse_out, float& dlt_out) {
       const int row = (i_begin + it) * 128 + static_cast<int>(r);
       lse_out = INFINITY, dlt_out = 0.0f;
-      if (it < n_it && row < a.Sq) {
+      if (it < n_it && row < a.Sq && ATTNQAT_IN_BOUNDS(static_cast<int64_t>(bh) * a.Sq + row < a.rows_q)) {
         lse_out = __ldg(a.lse + (size_t)bh * a.Sq + row);
         dlt_out = __ldg(a.delta + (size_t)bh * a.Sq + row);
       }
@@ -722,7 +725,7 @@ __global__ void __maxnreg__(128)
     auto row_stats = [&](int it, float& lse_out, float& dlt_out) {
       const int row = (i_begin + it) * 128 + static_cast<int>(r);
       lse_out = INFINITY, dlt_out = 0.0f;
-      if (it < n_it && row < a.Sq) {
+      if (it < n_it && row < a.Sq && ATTNQAT_IN_BOUNDS(static_cast<int64_t>(bh) * a.Sq + row < a.rows_q)) {
         lse_out = __ldg(a.lse + (size_t)bh * a.Sq + row);
         dlt_out = __ldg(a.delta + (size_t)bh * a.Sq + row);
       }
@@ -730,11 +733,16 @@ __global__ void __maxnreg__(128)
     // scale factors of K step `half`: K's are fixed; Q's follow the query tile
     auto q_scales = [&](int it, uint32_t (&w)[4]) {
       const int qt = i_begin + it;
-      if (it < n_it) load_scales(a.q_sf, qbase + qt * 128, min(128, a.Sq - qt * 128), static_cast<int>(half), w);
+      if (it < n_it)
+        load_scales(a.q_sf, qbase + qt * 128,
+                    ATTNQAT_IN_BOUNDS(qbase + qt * 128 + min(128, a.Sq - qt * 128) <= a.rows_q) ? min(128, a.Sq - qt * 128) : 0,
+                    static_cast<int>(half), w);
       else w[0] = w[1] = w[2] = w[3] = 0u;
     };
     uint32_t sfk[4], sfq[4];
-    load_scales(a.k_sf, kbase + j * 128, min(128, a.Sk - j * 128), static_cast<int>(half), sfk);
+    load_scales(a.k_sf, kbase + j * 128,
+                ATTNQAT_IN_BOUNDS(kbase + j * 128 + min(128, a.Sk - j * 128) <= a.rows_k) ? min(128, a.Sk - j * 128) : 0,
+                static_cast<int>(half), sfk);
     q_scales(0, sfq);
     tmem_st4(tmem + lane_off + 128 + 64 * half + L::kColSFQ, sfq);   // S(0)'s, in R1
     tmem_st4(tmem + lane_off + 128 + 64 * half + L::kColSFK, sfk);
@@ -890,6 +898,8 @@ cudaError_t launch_bwd(const Problem& p, const bf16* qh, const bf16* kh, const b
   const SplitPlan plan = bwd_split_plan(p, device_sm_count());
   a.n_full = static_cast<int>(plan.n_full);
   a.split_acc = split_acc, a.split_cnt = split_cnt;
+  ATTNQAT_CHECKED_ONLY(a.rows_q = static_cast<int64_t>(p.bh()) * p.Sq; a.rows_k = static_cast<int64_t>(p.bh()) * p.Sk;
+                       a.n_split = plan.n_split;)
   const int64_t blocks = plan.n_full + 2 * plan.n_split;
   if (blocks > 0x7fffffff || (plan.n_split > 0 && (split_acc == nullptr || split_cnt == nullptr)))
     return cudaErrorInvalidValue;
@@ -940,5 +950,8 @@ SplitPlan bwd_split_plan(const Problem& p, int sms) {
   if (s > kMaxSplitTiles) s = 0;
   return SplitPlan{tiles - s, s};
 }
+
+// the debug build's count of skipped accesses in this file's kernels
+ATTNQAT_OOB_READER(oob_read_bwd)
 
 }  // namespace attnqat

@@ -28,6 +28,7 @@
 // slows the softmax warps of its own sub-partition).
 // Shared memory: V^ x3, Q^, K^ x3.
 #include "attn_common.cuh"
+#include "checked.cuh"
 
 namespace attnqat {
 namespace {
@@ -84,6 +85,7 @@ struct FwdArgs {
   float c2;   // scale * log2(e)
   uint32_t* err;
   uint64_t timeout_ns;
+  ATTNQAT_CHECKED_ONLY(int64_t rows_q; int64_t rows_k;)   // debug build: B*H*Sq, B*H*Sk
 };
 
 __global__ void __launch_bounds__(kThreadsFwd, 1)
@@ -305,7 +307,8 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
         lse2 = M + lg2(Lsum);
         lse_s[r] = lse2;
         mbar_arrive(&B.lse_ready);
-        if (qrow < a.Sq) a.lse[(size_t)bh * a.Sq + qrow] = lse2 * kLn2;
+        if (qrow < a.Sq && ATTNQAT_IN_BOUNDS(static_cast<int64_t>(bh) * a.Sq + qrow < a.rows_q))
+          a.lse[(size_t)bh * a.Sq + qrow] = lse2 * kLn2;
       } else {
         ok = false;
       }
@@ -354,7 +357,8 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
       uint32_t v[32];
       const uint32_t col = (part & 1) * 32;
       tmem_ld32(tmem + lane_off + (part < 2 ? L::kColOP : L::kColO) + col, v);
-      if (qrow < a.Sq) store_row32_bf16((part < 2 ? a.o_hp : a.o) + row * kD + col, v, 1.0f);
+      if (qrow < a.Sq && ATTNQAT_IN_BOUNDS(static_cast<int64_t>(row) < a.rows_q))
+        store_row32_bf16((part < 2 ? a.o_hp : a.o) + row * kD + col, v, 1.0f);
     }
   }
 
@@ -394,11 +398,15 @@ cudaError_t launch_fwd(const Problem& p, const bf16* qh, const bf16* kh, const b
   a.causal = p.causal ? 1 : 0;
   a.c2 = p.scale * kLog2e;
   a.err = err, a.timeout_ns = wait_timeout_ns();
+  ATTNQAT_CHECKED_ONLY(a.rows_q = static_cast<int64_t>(p.bh()) * p.Sq; a.rows_k = static_cast<int64_t>(p.bh()) * p.Sk;)
   cudaError_t e = set_smem(reinterpret_cast<const void*>(&fwd_kernel), FwdLayout::kAlloc);
   if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>(a.n_qtiles), static_cast<unsigned>(bh));
   fwd_kernel<<<grid, kThreadsFwd, FwdLayout::kAlloc, st>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }
+
+// the debug build's count of skipped accesses in this file's kernels
+ATTNQAT_OOB_READER(oob_read_fwd)
 
 }  // namespace attnqat

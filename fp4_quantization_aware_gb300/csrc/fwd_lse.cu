@@ -33,6 +33,7 @@
 // producer; 9 MMA issuer (and TMEM allocation).
 #include "attn_common.cuh"
 #include "fp4_mma.cuh"
+#include "checked.cuh"
 
 namespace attnqat {
 namespace {
@@ -76,6 +77,7 @@ struct LseArgs {
   float c2;              // scale * log2(e)
   uint32_t* err;
   uint64_t timeout_ns;
+  ATTNQAT_CHECKED_ONLY(int64_t rows_q; int64_t rows_k;)   // debug build: B*H*Sq, B*H*Sk
 };
 
 // 32 TMEM columns of this warp's 32 lanes, without waiting.
@@ -248,7 +250,10 @@ __global__ void __launch_bounds__(kThreadsL, 1)
     const int64_t kbase = static_cast<int64_t>(bh) * a.Sk;
     auto k_scales = [&](int kt, uint32_t (&w)[2][4]) {
 #pragma unroll
-      for (int ks = 0; ks < 2; ++ks) load_scales(a.k_sf, kbase + kt * 128, min(128, a.Sk - kt * 128), ks, w[ks]);
+      for (int ks = 0; ks < 2; ++ks)
+        load_scales(a.k_sf, kbase + kt * 128,
+                    ATTNQAT_IN_BOUNDS(kbase + kt * 128 + min(128, a.Sk - kt * 128) <= a.rows_k) ? min(128, a.Sk - kt * 128) : 0,
+                    ks, w[ks]);
     };
     // Q scales of this warp's tile; K scales of key tiles 0, 1 (slots 0, 1)
     // from the scale writers. Every softmax thread arrives on sf_init.
@@ -257,7 +262,10 @@ __global__ void __launch_bounds__(kThreadsL, 1)
       uint32_t wq[2][4], wk[2][2][4];
 #pragma unroll
       for (int ks = 0; ks < 2; ++ks)
-        load_scales(a.q_sf, static_cast<int64_t>(bh) * a.Sq + qi * 128, min(128, a.Sq - qi * 128), ks, wq[ks]);
+        load_scales(a.q_sf, static_cast<int64_t>(bh) * a.Sq + qi * 128,
+                    ATTNQAT_IN_BOUNDS(static_cast<int64_t>(bh) * a.Sq + qi * 128 + min(128, a.Sq - qi * 128) <= a.rows_q)
+                        ? min(128, a.Sq - qi * 128) : 0,
+                    ks, wq[ks]);
       if (sf_writer) {
 #pragma unroll
         for (int kt = 0; kt < 2; ++kt)
@@ -345,7 +353,8 @@ __global__ void __launch_bounds__(kThreadsL, 1)
       ok = step(j, sfw, sfo);
       if (ok && j + 1 < nX) ok = step(j + 1, sfo, sfw);
     }
-    if (active && ok && qrow < a.Sq) a.lse[(size_t)bh * a.Sq + qrow] = (m + lg2(l)) * kLn2;
+    if (active && ok && qrow < a.Sq && ATTNQAT_IN_BOUNDS(static_cast<int64_t>(bh) * a.Sq + qrow < a.rows_q))
+      a.lse[(size_t)bh * a.Sq + qrow] = (m + lg2(l)) * kLn2;
   }
 
   tc_fence_before();
@@ -373,10 +382,14 @@ cudaError_t launch_fwd_lse(const Problem& p, const uint8_t* q4, const uint8_t* q
   a.causal = p.causal ? 1 : 0;
   a.c2 = p.scale * kLog2e;
   a.err = err, a.timeout_ns = wait_timeout_ns();
+  ATTNQAT_CHECKED_ONLY(a.rows_q = static_cast<int64_t>(p.bh()) * p.Sq; a.rows_k = static_cast<int64_t>(p.bh()) * p.Sk;)
   const dim3 grid(static_cast<unsigned>(a.n_pairs), static_cast<unsigned>(bh));
   cudaError_t e = set_smem(reinterpret_cast<const void*>(&fwd_lse_kernel), LseLayout::kAlloc);
   if (e != cudaSuccess) return e;
   return launch_dependent(fwd_lse_kernel, grid, dim3(kThreadsL), LseLayout::kAlloc, st, tq4, tk4, a);
 }
+
+// the debug build's count of skipped accesses in this file's kernels
+ATTNQAT_OOB_READER(oob_read_fwd_lse)
 
 }  // namespace attnqat

@@ -35,6 +35,7 @@
 // Shared memory: V^ x6 (16 KiB a tile), NVFP4 Q 8 KiB, NVFP4 K x6 (4 KiB).
 #include "attn_common.cuh"
 #include "fp4_mma.cuh"
+#include "checked.cuh"
 
 namespace attnqat {
 namespace {
@@ -115,6 +116,7 @@ struct PvArgs {
   float c2;                 // scale * log2(e)
   uint32_t* err;
   uint64_t timeout_ns;
+  ATTNQAT_CHECKED_ONLY(int64_t rows_q; int64_t rows_k; int64_t n_split;)   // debug build: B*H*Sq, B*H*Sk, split tiles
 };
 
 // 16 TMEM columns of this warp's 32 lanes, without waiting: tmem_wait_ld16
@@ -311,14 +313,19 @@ __global__ void __launch_bounds__(kThreadsV, 1)
     const int64_t kbase = static_cast<int64_t>(bh) * a.Sk;
     auto k_scales = [&](int t, uint32_t (&w)[4]) {   // this CTA's tile t; rows past the tile's 64 stay 0
       const int kt = kt0 + t;
-      load_scales(a.k_sf, kbase + static_cast<int64_t>(kt) * kKeysV, min(kKeysV, a.Sk - kt * kKeysV), ks, w);
+      const int rows = min(kKeysV, a.Sk - kt * kKeysV);
+      load_scales(a.k_sf, kbase + static_cast<int64_t>(kt) * kKeysV,
+                  ATTNQAT_IN_BOUNDS(kbase + static_cast<int64_t>(kt) * kKeysV + rows <= a.rows_k) ? rows : 0, ks, w);
     };
     // K scales written at tile t (those of tile t + 3), loaded one tile ahead.
     // The prologue issues all of its scale loads before the first TMEM store.
     uint32_t sfw[4] = {0u, 0u, 0u, 0u};
     if (sf_writer) {
       uint32_t w[1 + kRing][4];
-      load_scales(a.q_sf, static_cast<int64_t>(bh) * a.Sq + i * 128, min(128, a.Sq - i * 128), ks, w[0]);
+      load_scales(a.q_sf, static_cast<int64_t>(bh) * a.Sq + i * 128,
+                  ATTNQAT_IN_BOUNDS(static_cast<int64_t>(bh) * a.Sq + i * 128 + min(128, a.Sq - i * 128) <= a.rows_q)
+                      ? min(128, a.Sq - i * 128) : 0,
+                  ks, w[0]);
 #pragma unroll
       for (int kt = 0; kt < kRing; ++kt)
         if (kt < nt) k_scales(kt, w[1 + kt]);
@@ -332,7 +339,8 @@ __global__ void __launch_bounds__(kThreadsV, 1)
       mbar_arrive(&B.sf_init);
     }
     grid_dep_wait();
-    const float lse2 = qrow < a.Sq ? __ldg(a.lse + static_cast<size_t>(bh) * a.Sq + qrow) * kLog2e : 0.0f;
+    const float lse2 = qrow < a.Sq && ATTNQAT_IN_BOUNDS(static_cast<int64_t>(bh) * a.Sq + qrow < a.rows_q)
+                           ? __ldg(a.lse + static_cast<size_t>(bh) * a.Sq + qrow) * kLog2e : 0.0f;
     const float2 c22 = make_float2(a.c2, a.c2), nl = make_float2(-lse2, -lse2);
     // One tile: P = exp2(S c2 - lse2), P^ = fake_nvfp4(P) over this warp's S
     // columns, key tile t + 3's K scales from `sf_now` into their slot, key
@@ -459,7 +467,7 @@ __global__ void __launch_bounds__(kThreadsV, 1)
         bulk_wait_group<0>();        // this CTA's rows are written (and its staging read)
         fence_proxy_async_all();
         __threadfence();
-        B.split_order = atomicAdd(a.split_cnt + sidx, 1u);
+        B.split_order = ATTNQAT_IN_BOUNDS(sidx < a.n_split) ? atomicAdd(a.split_cnt + sidx, 1u) : 0u;
         if (B.split_order == 1u) {   // the other CTA's rows are written too
           __threadfence();
           fence_proxy_async_all();
@@ -548,6 +556,8 @@ cudaError_t launch_fwd_pv(const Problem& p, const bf16* vh, const uint8_t* q4, c
   const SplitPlan plan = fwd_pv_split_plan(p, device_sm_count());
   a.n_full = static_cast<int>(plan.n_full);
   a.split_acc = split_acc, a.split_cnt = split_cnt;
+  ATTNQAT_CHECKED_ONLY(a.rows_q = static_cast<int64_t>(p.bh()) * p.Sq; a.rows_k = static_cast<int64_t>(p.bh()) * p.Sk;
+                       a.n_split = plan.n_split;)
   const int64_t blocks = plan.n_full + 2 * plan.n_split;
   if (blocks > 0x7fffffff || (plan.n_split > 0 && (split_acc == nullptr || split_cnt == nullptr)))
     return cudaErrorInvalidValue;
@@ -582,5 +592,8 @@ SplitPlan fwd_pv_split_plan(const Problem& p, int sms) {
   if (s > kMaxSplitTiles) s = 0;
   return SplitPlan{tiles - s, s};
 }
+
+// the debug build's count of skipped accesses in this file's kernels
+ATTNQAT_OOB_READER(oob_read_fwd_pv)
 
 }  // namespace attnqat

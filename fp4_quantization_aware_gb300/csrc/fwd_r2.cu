@@ -32,6 +32,7 @@
 // PV(0) S(2) PV(1) ...; MMAs from one thread execute in issue order, so S(j+2)
 // overwrites buffer j % 2 only after PV(j) has read P(j) and P^(j) from it.
 #include "attn_common.cuh"
+#include "checked.cuh"
 #include "fp4_mma.cuh"
 
 namespace attnqat {
@@ -119,6 +120,7 @@ struct R2Args {
   float c2;   // scale * log2(e)
   uint32_t* err;
   uint64_t timeout_ns;
+  ATTNQAT_CHECKED_ONLY(int64_t rows_q; int64_t rows_k;)   // debug build: B*H*Sq, B*H*Sk
 };
 
 template <int D, int PF>
@@ -377,11 +379,14 @@ __global__ void __launch_bounds__(kThreadsR2, 1)
         const uint32_t col = half * (D / 2) + c * 32;
         uint32_t o[32];
         tmem_ld32(tmem + lane_off + L::kColOP + col, o);
-        if (qrow < a.Sq) store_row32_bf16(a.o_hp + row * D + col, o, inv);
+        if (qrow < a.Sq && ATTNQAT_IN_BOUNDS(static_cast<int64_t>(row) < a.rows_q))
+          store_row32_bf16(a.o_hp + row * D + col, o, inv);
         tmem_ld32(tmem + lane_off + L::kColO + col, o);
-        if (qrow < a.Sq) store_row32_bf16(a.o + row * D + col, o, inv);
+        if (qrow < a.Sq && ATTNQAT_IN_BOUNDS(static_cast<int64_t>(row) < a.rows_q))
+          store_row32_bf16(a.o + row * D + col, o, inv);
       }
-      if (half == 0 && qrow < a.Sq) a.lse[row] = (mref + lg2(ltot)) * kLn2;
+      if (half == 0 && qrow < a.Sq && ATTNQAT_IN_BOUNDS(static_cast<int64_t>(row) < a.rows_q))
+        a.lse[row] = (mref + lg2(ltot)) * kLn2;
     }
   }
 
@@ -430,9 +435,13 @@ cudaError_t launch_fwd_r2(const Problem& p, const bf16* qh, const bf16* kh, cons
   a.causal = p.causal ? 1 : 0;
   a.c2 = p.scale * kLog2e;
   a.err = err, a.timeout_ns = wait_timeout_ns();
+  ATTNQAT_CHECKED_ONLY(a.rows_q = static_cast<int64_t>(p.bh()) * p.Sq; a.rows_k = static_cast<int64_t>(p.bh()) * p.Sk;)
   const dim3 grid(static_cast<unsigned>(a.n_qtiles), static_cast<unsigned>(bh));
   return p.D == 128 ? launch_r2_fmt<128>(tq, tk, tv, a, grid, p_format, st)
                     : launch_r2_fmt<64>(tq, tk, tv, a, grid, p_format, st);
 }
+
+// the debug build's count of skipped accesses in this file's kernels
+ATTNQAT_OOB_READER(oob_read_fwd_r2)
 
 }  // namespace attnqat

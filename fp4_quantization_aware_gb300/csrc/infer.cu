@@ -32,6 +32,7 @@
 // K scales x2 [400,408) and [416,424). Warps: 0-7 softmax, 8 TMA producer,
 // 9 PV issuer, 10 S issuer.
 #include "attn_common.cuh"
+#include "checked.cuh"
 #include "fp4_mma.cuh"
 
 namespace attnqat {
@@ -96,6 +97,7 @@ struct InfArgs {
   float c2;               // scale * log2(e)
   uint32_t* err;
   uint64_t timeout_ns;
+  ATTNQAT_CHECKED_ONLY(int64_t rows_q; int64_t rows_k;)   // debug build: B*H*Sq, B*H*Sk
 };
 
 // Three warps share SM sub-partitions 0-2: at most 168 registers a thread.
@@ -236,12 +238,12 @@ __global__ void __maxnreg__(168)
     const int64_t qbase = static_cast<int64_t>(bh) * a.Sq, kbase = static_cast<int64_t>(bh) * a.Sk;
     {
       uint32_t w[4];
-      load_scales(a.q_sf, qbase + i * 128, min(128, a.Sq - i * 128), half, w);
+      load_scales(a.q_sf, qbase + i * 128, ATTNQAT_IN_BOUNDS(qbase + i * 128 + min(128, a.Sq - i * 128) <= a.rows_q) ? min(128, a.Sq - i * 128) : 0, half, w);
       tmem_st4(tmem + lane_off + L::kColSFQ + 4 * half, w);
-      load_scales(a.k_sf, kbase, min(128, a.Sk), half, w);
+      load_scales(a.k_sf, kbase, ATTNQAT_IN_BOUNDS(kbase + min(128, a.Sk) <= a.rows_k) ? min(128, a.Sk) : 0, half, w);
       tmem_st4(tmem + lane_off + L::kColSFK0 + 4 * half, w);
       if (nk > 1) {
-        load_scales(a.k_sf, kbase + 128, min(128, a.Sk - 128), half, w);
+        load_scales(a.k_sf, kbase + 128, ATTNQAT_IN_BOUNDS(kbase + 128 + min(128, a.Sk - 128) <= a.rows_k) ? min(128, a.Sk - 128) : 0, half, w);
         tmem_st4(tmem + lane_off + L::kColSFK1 + 4 * half, w);
       }
       tc_fence_before();
@@ -255,7 +257,9 @@ __global__ void __maxnreg__(168)
       const int b = j & 1;
       const bool more = j + 2 < nk;
       uint32_t sfw[4] = {0u, 0u, 0u, 0u};
-      if (more) load_scales(a.k_sf, kbase + (j + 2) * 128, min(128, a.Sk - (j + 2) * 128), half, sfw);
+      if (more)
+        load_scales(a.k_sf, kbase + (j + 2) * 128,
+                    ATTNQAT_IN_BOUNDS(kbase + (j + 2) * 128 + min(128, a.Sk - (j + 2) * 128) <= a.rows_k) ? min(128, a.Sk - (j + 2) * 128) : 0, half, sfw);
       const uint32_t scol = tmem + lane_off + L::kColS0 + b * 128 + 64 * half;
       uint32_t v[64];
       const bool got = !fail && warp_wait(&B.s_full[b], (j >> 1) & 1, ctl);
@@ -352,9 +356,10 @@ __global__ void __maxnreg__(168)
       for (int c = 0; c < 2; ++c) {
         uint32_t o[32];
         tmem_ld32(tmem + lane_off + L::kColO + 64 * half + 32 * c, o);
-        if (qrow < a.Sq) store_row32_bf16(out + 32 * c, o, inv);
+        if (qrow < a.Sq && ATTNQAT_IN_BOUNDS(qbase + qrow < a.rows_q)) store_row32_bf16(out + 32 * c, o, inv);
       }
-      if (half == 0 && a.lse != nullptr && qrow < a.Sq) a.lse[qbase + qrow] = (mref + lg2(ltot)) * kLn2;
+      if (half == 0 && a.lse != nullptr && qrow < a.Sq && ATTNQAT_IN_BOUNDS(qbase + qrow < a.rows_q))
+        a.lse[qbase + qrow] = (mref + lg2(ltot)) * kLn2;
     }
   }
 
@@ -384,11 +389,15 @@ cudaError_t launch_infer(const Problem& p, const uint8_t* q_fp4, const uint8_t* 
   a.causal = p.causal ? 1 : 0;
   a.c2 = p.scale * kLog2e;
   a.err = err, a.timeout_ns = wait_timeout_ns();
+  ATTNQAT_CHECKED_ONLY(a.rows_q = static_cast<int64_t>(p.bh()) * p.Sq; a.rows_k = static_cast<int64_t>(p.bh()) * p.Sk;)
   cudaError_t e = set_smem(reinterpret_cast<const void*>(&infer_kernel), InfLayout::kAlloc);
   if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>(a.n_qtiles), static_cast<unsigned>(bh));
   infer_kernel<<<grid, kThreadsInf, InfLayout::kAlloc, st>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }
+
+// the debug build's count of skipped accesses in this file's kernels
+ATTNQAT_OOB_READER(oob_read_infer)
 
 }  // namespace attnqat

@@ -58,6 +58,20 @@ cudaError_t launch_nvfp4_pack(const bf16* x, uint8_t* packed, uint8_t* scales, i
 
 cudaError_t launch_dq_convert(const Problem& p, const float* dq_acc, bf16* dq, cudaStream_t st);
 
+// The debug build (ATTNQAT_CHECKED, checked.cuh): each file's count of the
+// accesses its bounds checks skipped (added to *out; cleared when asked; the
+// product build's readers add nothing), and the checks' self-test, which
+// writes n + extra elements of an n-element buffer (product build:
+// cudaErrorNotSupported, nothing launched).
+cudaError_t oob_read_fwd_lse(unsigned long long* out, bool clear);
+cudaError_t oob_read_fwd_pv(unsigned long long* out, bool clear);
+cudaError_t oob_read_fwd(unsigned long long* out, bool clear);
+cudaError_t oob_read_fwd_r2(unsigned long long* out, bool clear);
+cudaError_t oob_read_bwd(unsigned long long* out, bool clear);
+cudaError_t oob_read_infer(unsigned long long* out, bool clear);
+cudaError_t oob_read_quant(unsigned long long* out, bool clear);
+cudaError_t launch_bounds_selftest(float* buf, int64_t n, int64_t extra, cudaStream_t st);
+
 // The forward; q4, qsf, k4, ksf: NVFP4 Q and K for the first pass's
 // block-scaled S (D = 128; null for D = 64, which stays on BF16).
 cudaError_t launch_fwd(const Problem& p, const bf16* qh, const bf16* kh, const bf16* vh, const uint8_t* q4,

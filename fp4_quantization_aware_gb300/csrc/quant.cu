@@ -13,6 +13,7 @@
 // conversion gives a thread four float4s a block apart, loaded first.
 #include "kernels.h"
 #include "nvfp4.cuh"
+#include "checked.cuh"
 
 namespace attnqat {
 namespace {
@@ -184,6 +185,17 @@ __global__ void __launch_bounds__(kThreads) dq_convert_kernel(const float4* __re
     if (i0 + u * kThreads < n4)
       dq[i0 + u * kThreads] = make_uint2(pack_bf16x2(v[u].x, v[u].y), pack_bf16x2(v[u].z, v[u].w));
 }
+
+// The debug build's self-test of its bounds checks: thread i of n + extra
+// writes element i of an n-element buffer behind the same guard as the
+// kernels' accesses, so the extra threads' writes are skipped and counted.
+// Only the debug build has it.
+#ifdef ATTNQAT_CHECKED
+__global__ void __launch_bounds__(kThreads) bounds_selftest_kernel(float* buf, int64_t n, int64_t total) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+  if (i < total && ATTNQAT_IN_BOUNDS(i < n)) buf[i] = static_cast<float>(i);
+}
+#endif
 
 // One CTA waits on a barrier that nothing arrives at; the bounded wait gives
 // up after timeout_ns, records the error and the kernel returns.
@@ -365,9 +377,24 @@ cudaError_t launch_quotient_selftest(unsigned long long* out, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+cudaError_t launch_bounds_selftest(float* buf, int64_t n, int64_t extra, cudaStream_t st) {
+#ifdef ATTNQAT_CHECKED
+  const int64_t total = n + extra;
+  if (n < 0 || extra < 0 || total == 0) return cudaErrorInvalidValue;
+  bounds_selftest_kernel<<<blocks_for(total), kThreads, 0, st>>>(buf, n, total);
+  return cudaGetLastError();
+#else
+  (void)buf, (void)n, (void)extra, (void)st;
+  return cudaErrorNotSupported;   // no guard in the product build: never launched
+#endif
+}
+
 cudaError_t launch_wait_timeout(uint32_t* err, uint64_t timeout_ns, cudaStream_t st) {
   wait_timeout_kernel<<<1, 32, 0, st>>>(err, timeout_ns);
   return cudaGetLastError();
 }
+
+// the debug build's count of skipped accesses in this file's kernels
+ATTNQAT_OOB_READER(oob_read_quant)
 
 }  // namespace attnqat

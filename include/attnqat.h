@@ -320,6 +320,27 @@ attnqat_status attnqat_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
  * use concurrently with other calls. */
 attnqat_status attnqat_selftest_set_wait_limit(uint64_t timeout_ns);
 
+/* ---- debug build (libattnqat_checked.so, compiled with ATTNQAT_CHECKED) ----
+ * Every plain global load and store of the attention kernels (TMA copies are
+ * clipped by their tensor maps) checks that its element index lies inside the
+ * extent of the buffer it addresses; an access that would not is skipped and
+ * counted in device counters, so a bad index shows up as a count, never as a
+ * fault. No page defines these; they stand in for a memory checker. */
+
+/* 1 in the debug build, 0 in the product build (libattnqat.so). */
+int attnqat_checked_build(void);
+
+/* The number of accesses the debug build's checks skipped since the last
+ * clear (synchronizes the device; clear != 0 resets the counters). The product
+ * build returns ATTNQAT_ERR_UNSUPPORTED. */
+attnqat_status attnqat_debug_oob_count(unsigned long long* count, int clear);
+
+/* Self-test of the checks: n + extra threads each write one element of the
+ * n-element device buffer buf (float) behind the same guard, so the last
+ * `extra` writes are skipped and counted (read with attnqat_debug_oob_count).
+ * The product build returns ATTNQAT_ERR_UNSUPPORTED and launches nothing. */
+attnqat_status attnqat_selftest_bounds(float* buf, int64_t n, int64_t extra, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

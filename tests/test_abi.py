@@ -34,6 +34,23 @@ def test_every_declared_symbol_is_exported(clib):
     assert set(names) == set(attnqat.SIGNATURES), "binding and header disagree"
 
 
+def test_debug_build_exports_the_same_symbols_and_says_so(clib):
+    builder.build(checked=True)
+    raw = ctypes.CDLL(attnqat.CHECKED_LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(raw, n)]
+    assert not missing, missing
+    raw.attnqat_checked_build.restype = ctypes.c_int
+    assert raw.attnqat_checked_build() == 1
+    assert clib.attnqat_checked_build() == 0
+
+
+def test_product_build_has_no_bounds_checks(clib):
+    n = ctypes.c_ulonglong(7)
+    assert clib.attnqat_debug_oob_count(ctypes.byref(n), 0) == 2            # unsupported
+    assert clib.attnqat_selftest_bounds(None, 16, 4, None) == 2             # nothing launched
+    assert b"debug build" in clib.attnqat_last_error_message()
+
+
 def test_version_and_status_strings(clib):
     assert clib.attnqat_version() >= 100
     assert clib.attnqat_status_string(0) == b"ok"
