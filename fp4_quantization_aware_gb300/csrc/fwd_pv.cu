@@ -372,12 +372,18 @@ __global__ void __launch_bounds__(kThreadsV, 1)
           for (int k = 0; k < 16; ++k)
             if (16 * g + k >= valid) P[k] = 0.0f;
         }
-        uint32_t pw[8], phw[8];
+        // P in words 0-7, P^ in words 8-15: with one group per warp their
+        // columns (8 g and 8 kGroups + 8 g) are adjacent, one 16-column store
+        uint32_t pw[16];
 #pragma unroll
         for (int k = 0; k < 8; ++k) pw[k] = pack_bf16x2(P[2 * k], P[2 * k + 1]);
-        fake_nvfp4_16_pack_nonneg<false>(P, 1.0f, phw);
-        tmem_st8_nowait(pcol + 8 * g, pw);
-        tmem_st8_nowait(pcol + 8 * kGroups + 8 * g, phw);
+        fake_nvfp4_16_pack_nonneg<false>(P, 1.0f, pw + 8);
+        if constexpr (kGroups == 1) {
+          tmem_st16_nowait(pcol, pw);
+        } else {
+          tmem_st8_nowait(pcol + 8 * g, pw);
+          tmem_st8_nowait(pcol + 8 * kGroups + 8 * g, pw + 8);
+        }
       }
       // key tile t + 3's K scales into slot (t + 3) % 4, last read by S(t - 1),
       // which is complete since S(t) is; S(t + 3) is issued only after the
