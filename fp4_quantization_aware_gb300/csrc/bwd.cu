@@ -807,9 +807,12 @@ __global__ void __maxnreg__(128)
           if (h == 0 && it > 0) df = warp_poll(&B.ds_free, (it - 1) & 1);
           if (h == 1 && it + 1 < n_it) {
             // dP(it) is read: S(it+1)'s scale factors go over its last 8
-            // columns of this half, and S(it+1) may start
-            tmem_st4(tmem + lane_off + reg + L::kColSFQ, sfq);
-            tmem_st4(tmem + lane_off + reg + L::kColSFK, sfk);
+            // columns of this half (Q's then K's, adjacent: one store, one
+            // wait), and S(it+1) may start
+            static_assert(L::kColSFK == L::kColSFQ + 4, "Q and K scale columns adjacent");
+            const uint32_t sf8[8] = {sfq[0], sfq[1], sfq[2], sfq[3], sfk[0], sfk[1], sfk[2], sfk[3]};
+            tmem_st8_nowait(tmem + lane_off + reg + L::kColSFQ, sf8);
+            tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&B.sf_ready);
             q_scales(it + 2, sfq);
